@@ -1,0 +1,216 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the row-wise
+ * reduce-then-rescale operations: RMSNorm, fused residual-add + RMSNorm and
+ * safe softmax.
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the timed
+ * CPU-baseline leg of the benchmark load the library built from this file.
+ * The CUDA library never calls it, and the two share no source, header,
+ * table or helper.  Every function here is a direct restatement of a
+ * definition printed on the pages cited beside it; nothing is blocked, fused
+ * or reordered beyond what that definition states.  All arithmetic is IEEE
+ * binary64; the only narrowing is the explicit, single rounding of a binary64
+ * result to the storage type (binary32 or bfloat16), round-to-nearest-even.
+ *
+ * Pages cited (by title and section):
+ *   [KJ]  "RMSNorm、Softmax 与在线归约" (notes.kuangjux.top)
+ *   [DY]  "两个融合算子：RMSNorm 与 online softmax" (daleiyang.github.io)
+ *   [AZ]  "GPU Kernel 工程（04）：共享内存与 reduction——softmax、LayerNorm
+ *          与 online softmax" (arganzheng.life)
+ *   [AR]  "Softmax 与归一化", CUDA 进阶手册 (anrans.github.io)
+ *
+ * Storage types: 0 = binary32, 1 = bfloat16 (the upper 16 bits of a binary32).
+ * Every function takes rows stored contiguously, row-major, row stride equal
+ * to the row length, and writes binary64 results.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+static int g_threads = 1;
+
+/* Number of host threads used over rows (rows are independent, so this does
+ * not change any result). */
+void orc_set_threads(int n) { g_threads = n > 0 ? n : 1; }
+int orc_get_threads(void) { return g_threads; }
+
+/* Value of element i of a binary32 or bfloat16 array, exactly, as binary64. */
+static double elem(const void *p, int dt, int64_t i) {
+    if (dt == ORC_F32) return (double)((const float *)p)[i];
+    uint32_t u = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a binary64 value once, to nearest with ties to even, to bfloat16
+ * (8 significant bits, exponent range of binary32).  Returns the 16-bit
+ * pattern.  Near v the bfloat16 values are spaced 2^(e-8), where
+ * v = f * 2^e with 0.5 <= |f| < 1; below the normal range (e < -125) the
+ * spacing stays at the subnormal quantum 2^-133. */
+uint16_t orc_round_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    if (isinf(v)) return v < 0 ? 0xFF80 : 0x7F80;
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+    int e;
+    frexp(v, &e);
+    if (e < -125) e = -125;
+    double q = ldexp(1.0, e - 8);
+    double r = nearbyint(v / q) * q; /* default rounding mode: ties to even */
+    if (fabs(r) >= 0x1p128) return v < 0 ? 0xFF80 : 0x7F80;
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Round a binary64 value once to the storage type and return that stored
+ * value as binary64. */
+static double round_to(double v, int dt) {
+    if (dt == ORC_F32) return (double)(float)v;
+    uint32_t u = (uint32_t)orc_round_bf16(v) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Store n binary64 values into a binary32 or bfloat16 array, each rounded
+ * once to nearest-even. */
+void orc_round_array(const double *v, int64_t n, int dt, void *out) {
+    for (int64_t i = 0; i < n; ++i) {
+        if (dt == ORC_F32)
+            ((float *)out)[i] = (float)v[i];
+        else
+            ((uint16_t *)out)[i] = orc_round_bf16(v[i]);
+    }
+}
+
+/* RMSNorm of one row, definition of [KJ] "RMSNorm 归约什么" and [AZ] 八.1:
+ *   r = (mean_j x_j^2 + eps)^(-1/2),   y_j = x_j * r * gamma_j
+ * eps sits inside the square root; the mean divides by H.  `h` holds the row
+ * as binary64. */
+static void rmsnorm_row(const double *h, const void *gamma, int dt, double eps,
+                        int64_t H, double *y, double *rstd) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < H; ++j) ss += h[j] * h[j];
+    double r = 1.0 / sqrt(ss / (double)H + eps);
+    for (int64_t j = 0; j < H; ++j) y[j] = h[j] * r * elem(gamma, dt, j);
+    if (rstd) *rstd = r;
+}
+
+/* y[M][H] = RMSNorm(x) * gamma; rstd[M] (optional) = r of each row. */
+void orc_rmsnorm(const void *x, const void *gamma, int dt, double eps, int64_t M,
+                 int64_t H, double *y, double *rstd) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double *h = y + i * H; /* the row is widened into its output slot */
+        for (int64_t j = 0; j < H; ++j) h[j] = elem(x, dt, i * H + j);
+        rmsnorm_row(h, gamma, dt, eps, H, h, rstd ? rstd + i : 0);
+    }
+}
+
+/* Fused residual-add + RMSNorm, [AZ] 八.3 and [AR] "RMSNorm" fused variant:
+ *   h = x + residual          (stored back as the new residual, rounded once
+ *                              to the storage type)
+ *   out = RMSNorm(h) * gamma  (of the stored, rounded h)
+ * h_out[M][H] receives the new residual (values exactly representable in the
+ * storage type), y[M][H] the normalised output before its final rounding. */
+void orc_fused_add_rmsnorm(const void *x, const void *residual, const void *gamma,
+                           int dt, double eps, int64_t M, int64_t H, double *h_out,
+                           double *y, double *rstd) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double *h = h_out + i * H;
+        for (int64_t j = 0; j < H; ++j)
+            h[j] = round_to(elem(x, dt, i * H + j) + elem(residual, dt, i * H + j), dt);
+        rmsnorm_row(h, gamma, dt, eps, H, y + i * H, rstd ? rstd + i : 0);
+    }
+}
+
+/* Safe softmax, three passes, [KJ] "稳定 Softmax" and [AZ] 七.2:
+ *   m = max_j x_j,  d = sum_j exp(x_j - m),  y_i = exp(x_i - m) / d.
+ * m_out/d_out (optional) receive m and d of each row. */
+void orc_softmax(const void *x, int dt, int64_t M, int64_t N, double *y,
+                 double *m_out, double *d_out) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            double v = elem(x, dt, i * N + j);
+            if (v > m) m = v;
+        }
+        double d = 0.0;
+        for (int64_t j = 0; j < N; ++j) d += exp(elem(x, dt, i * N + j) - m);
+        for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + j) - m) / d;
+        if (m_out) m_out[i] = m;
+        if (d_out) d_out[i] = d;
+    }
+}
+
+/* Online normaliser, one element at a time, [KJ] "Online Softmax 为什么要重缩放
+ * 旧的和" and [AR] "Online softmax": start from the first element as (x_1, 1);
+ * for each further x:  m' = max(m, x),  d <- d * exp(m - m') + exp(x - m'),
+ * m <- m'.  Then y_i = exp(x_i - m) / d.  Defined for non-empty finite rows. */
+void orc_softmax_online(const void *x, int dt, int64_t M, int64_t N, double *y,
+                        double *m_out, double *d_out) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double m = elem(x, dt, i * N), d = 1.0;
+        for (int64_t j = 1; j < N; ++j) {
+            double v = elem(x, dt, i * N + j);
+            double mn = v > m ? v : m;
+            d = d * exp(m - mn) + exp(v - mn);
+            m = mn;
+        }
+        for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + j) - m) / d;
+        if (m_out) m_out[i] = m;
+        if (d_out) d_out[i] = d;
+    }
+}
+
+/* Merge of two (m, d) summaries, [DY] §5·三 "结合律" and [KJ] "从逐元素更新到
+ * 合并两个 tile":  m = max(m1, m2),  d = d1 * exp(m1 - m) + d2 * exp(m2 - m). */
+void orc_md_merge(double m1, double d1, double m2, double d2, double *m, double *d) {
+    double mm = m1 > m2 ? m1 : m2;
+    *m = mm;
+    *d = d1 * exp(m1 - mm) + d2 * exp(m2 - mm);
+}
+
+/* Row statistics by chunk summaries, [DY] §4·四 "S4": each run of `chunk`
+ * consecutive elements is summarised on its own (its max, then the sum of
+ * exp(x - that max)), and the summaries are merged left to right with the
+ * (m, d) merge above.  Used only to check that chunking does not change the
+ * statistics. */
+void orc_softmax_chunked_stats(const void *x, int dt, int64_t M, int64_t N,
+                               int64_t chunk, double *m_out, double *d_out) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double m = -INFINITY, d = 0.0;
+        int first = 1;
+        for (int64_t c0 = 0; c0 < N; c0 += chunk) {
+            int64_t c1 = c0 + chunk < N ? c0 + chunk : N;
+            double cm = -INFINITY;
+            for (int64_t j = c0; j < c1; ++j) {
+                double v = elem(x, dt, i * N + j);
+                if (v > cm) cm = v;
+            }
+            double cd = 0.0;
+            for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - cm);
+            if (first) {
+                m = cm;
+                d = cd;
+                first = 0;
+            } else {
+                orc_md_merge(m, d, cm, cd, &m, &d);
+            }
+        }
+        m_out[i] = m;
+        d_out[i] = d;
+    }
+}

@@ -1,0 +1,123 @@
+"""Seeded synthetic inputs for the row-wise reduce-then-rescale workloads.
+
+This module holds only input generation: shapes, value distributions and
+structure (shifted rows, spikes).  It contains none of the arithmetic of
+RMSNorm or softmax, and both the fp64 oracle's tests and the CUDA path's
+tests and benchmark draw their inputs from it.
+
+Recipe (every workload): one ``torch.Generator`` seeded with ``seed``
+(default 0) on the requested device; binary32 samples are drawn in the order
+x, residual, gamma, then the structure (shifted rows, spike columns); the cast
+to bfloat16 (round-to-nearest-even) comes last.  Shapes follow the Qwen2.5-7B
+numbers the pages use (hidden 3584, 28 heads, vocabulary 152064).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+ELEM_BYTES = {"f32": 4, "bf16": 2}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "softmax"
+    M: int
+    N: int                  # row length (H for the norms)
+    in_dtype: str
+    out_dtype: str
+    sigma: float = 1.0      # std of the normal samples
+    eps: float = 1e-6
+    shift_rows: int = 0     # rows that get +shift added (softmax overflow check)
+    shift: float = 1000.0
+    spikes_per_row: int = 0
+    spike: float = 30.0
+    l2_resident: bool = False
+    note: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def min_bytes(self) -> int:
+        """Minimum HBM traffic of one call: each input read once, each output
+        written once, gamma counted once."""
+        e_in, e_out = ELEM_BYTES[self.in_dtype], ELEM_BYTES[self.out_dtype]
+        n = self.M * self.N
+        if self.op == "rmsnorm":
+            return n * e_in + n * e_out + self.N * e_in
+        if self.op == "fused_add_rmsnorm":
+            return 2 * n * e_in + 2 * n * e_out + self.N * e_in
+        return n * e_in + n * e_out
+
+
+SWEEP_N = (32, 128, 1024, 4096, 32768, 152064)
+
+WORKLOADS = {
+    "rmsnorm_f32_64x3584": Workload(
+        "rmsnorm_f32_64x3584", "rmsnorm", 64, 3584, "f32", "f32", sigma=1.0,
+        l2_resident=True, note="RMSNorm fp32, 64 rows x hidden 3584"),
+    "fused_add_rmsnorm_bf16_8192x4096": Workload(
+        "fused_add_rmsnorm_bf16_8192x4096", "fused_add_rmsnorm", 8192, 4096, "bf16", "bf16",
+        sigma=1.0, note="fused residual-add + RMSNorm bf16, batch 4 x seq 2048 x hidden 4096"),
+    "softmax_attn_f32_114688x4096": Workload(
+        "softmax_attn_f32_114688x4096", "softmax", 28 * 4096, 4096, "f32", "f32", sigma=3.0,
+        shift_rows=round(0.01 * 28 * 4096),
+        note="attention-score softmax fp32, 28 heads x 4096 queries x 4096 keys, 1% rows +1000"),
+    "softmax_vocab_bf16_f32_64x152064": Workload(
+        "softmax_vocab_bf16_f32_64x152064", "softmax", 64, 152064, "bf16", "f32", sigma=4.0,
+        spikes_per_row=8, l2_resident=True,
+        note="vocabulary-logit softmax, bf16 in / fp32 out, 64 rows x 152064, 8 spikes +30 per row"),
+}
+for _n in SWEEP_N:
+    _name = f"softmax_sweep_f32_N{_n}"
+    WORKLOADS[_name] = Workload(_name, "softmax", (1 << 26) // _n, _n, "f32", "f32", sigma=2.0,
+                                note=f"softmax fp32 sweep, 256 MiB per tensor, N={_n}")
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def rmsnorm_inputs(M, H, dtype="f32", sigma=1.0, fused=False, seed=0, device="cpu"):
+    """x (and residual) ~ N(0, sigma^2), gamma ~ U(0.5, 1.5)."""
+    g = _gen(device, seed)
+    x = torch.randn(M, H, generator=g, device=device, dtype=torch.float32) * sigma
+    res = None
+    if fused:
+        res = torch.randn(M, H, generator=g, device=device, dtype=torch.float32) * sigma
+    gamma = torch.rand(H, generator=g, device=device, dtype=torch.float32) + 0.5
+    out = {"x": x.to(_DT[dtype]), "gamma": gamma.to(_DT[dtype])}
+    if fused:
+        out["residual"] = res.to(_DT[dtype])
+    return out
+
+
+def softmax_inputs(M, N, dtype="f32", sigma=1.0, shift_rows=0, shift=1000.0,
+                   spikes_per_row=0, spike=30.0, seed=0, device="cpu"):
+    """x ~ N(0, sigma^2); `shift_rows` distinct rows (seeded permutation) get
+    +shift; each row gets `spikes_per_row` distinct seeded columns +spike."""
+    g = _gen(device, seed)
+    x = torch.randn(M, N, generator=g, device=device, dtype=torch.float32) * sigma
+    if shift_rows:
+        rows = torch.randperm(M, generator=g, device=device)[:shift_rows]
+        x[rows] += shift
+    if spikes_per_row:
+        for r in range(M):
+            cols = torch.randperm(N, generator=g, device=device)[:spikes_per_row]
+            x[r, cols] += spike
+    return {"x": x.to(_DT[dtype])}
+
+
+def make(w: Workload | str, seed=0, device="cpu"):
+    """Inputs of a named workload, as torch tensors on `device`."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    if w.op in ("rmsnorm", "fused_add_rmsnorm"):
+        return rmsnorm_inputs(w.M, w.N, w.in_dtype, w.sigma, w.op == "fused_add_rmsnorm",
+                              seed, device)
+    return softmax_inputs(w.M, w.N, w.in_dtype, w.sigma, w.shift_rows, w.shift,
+                          w.spikes_per_row, w.spike, seed, device)
