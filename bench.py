@@ -1,0 +1,482 @@
+"""Benchmark of the row-wise reduce-then-rescale kernels on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-suite]
+
+Prints ONE JSON line.  Metric: achieved HBM bandwidth counting minimum bytes
+(each input read once, each output written once, gamma once) and its fraction
+of the GB300 HBM peak.  A step is one call of the operation over the
+workload's whole batch; the default workload is the fused residual-add +
+RMSNorm, bf16, 8192 x 4096.  `per_kernel` repeats the measurement for every
+named workload (RMSNorm, fused, attention softmax, vocabulary softmax and the
+row-length sweep), one dispatcher leaf each.
+
+Inputs are resident in HBM; consecutive steps rotate over enough distinct
+input/output sets that no step finds its data in L2 (more than twice the L2
+capacity of traffic between two uses of a set).  Device time comes from CUDA
+events on the launching stream around the K timed steps.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(rows are independent: weak scaling, no collective on the data path); the
+reported time is the maximum over ranks.
+
+`--impl reference` times the fp64 CPU oracle (the only reference there is)
+on bounded samples of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "achieved HBM GB/s (min bytes) and % of GB300 HBM peak per kernel, 1 GPU"
+NOMINAL_HBM_GBS = 8000.0          # NVIDIA's public per-GPU HBM3e figure for GB300
+FALLBACK_HBM_GBS = 6800.0         # used only when no measured peak file exists
+DEFAULT_WORKLOAD = "fused_add_rmsnorm_bf16_8192x4096"
+OP_CODE = {"rmsnorm": 0, "fused_add_rmsnorm": 1, "softmax": 2}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate_over_ranks(elapsed_ms: float, units: float, world: int):
+    """Max of the per-rank elapsed times and the sum of units over ranks
+    (whole-job throughput = sum of units / slowest rank's time)."""
+    if world > 1 and torch.distributed.is_initialized():
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        u = torch.tensor([units], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+        return float(t.item()), float(u.item())
+    return elapsed_ms, units
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: torch copy, 2 GiB)"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "online_softmax_row_gb300", "csrc", "*")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the workload's kernel from the committed ncu
+    summary (profiles/dram_traffic.md), if it was captured on the current
+    kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = source_hash()
+    for line in open(path, encoding="utf-8"):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == want:
+            try:
+                return int(cells[3].replace(",", ""))
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            self.proc = subprocess.Popen([exe, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            c = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(c[1]))
+                smax.append(float(c[2]))
+                power.append(float(c[3]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, c[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def make_sets(w, n_sets, device):
+    """n_sets independent input/output sets of workload w, on device."""
+    sets = []
+    for i in range(n_sets):
+        inp = workloads.make(w, seed=i, device=device)
+        s = dict(inp)
+        if w.op == "softmax":
+            s["y"] = torch.empty(w.M, w.N, dtype=DT[w.out_dtype], device=device)
+        else:
+            s["y"] = torch.empty_like(inp["x"])
+        sets.append(s)
+    return sets
+
+
+def n_sets_for(w, l2_bytes):
+    per_set = w.min_bytes
+    return max(2, math.ceil(2 * l2_bytes / max(per_set, 1)) + 1)
+
+
+def call(osr, w, s):
+    if w.op == "softmax":
+        return osr.softmax_rows(s["x"], out=s["y"])
+    if w.op == "rmsnorm":
+        return osr.rmsnorm_fwd(s["x"], s["gamma"], w.eps, out=s["y"])
+    return osr.fused_add_rmsnorm(s["x"], s["residual"], s["gamma"], w.eps, out=s["y"])
+
+
+def launches_per_call(plan: str, M: int) -> int:
+    if plan.startswith("split"):
+        b = int(re.search(r"b=(\d+)", plan).group(1))
+        return 2 * math.ceil(M / b)
+    return 1
+
+
+def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, sustain_s=0.0):
+    """Device time of `steps` back-to-back calls (rotating input sets)."""
+    sets = make_sets(w, n_sets_for(w, l2_bytes), device)
+    stream = torch.cuda.current_stream(device)
+    for i in range(max(warmup, 3)):
+        call(osr, w, sets[i % len(sets)])
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    clocks = None
+
+    def sustain():
+        if sustain_s <= 0:
+            return
+        t_end = time.time() + sustain_s
+        i = 0
+        while time.time() < t_end:
+            for _ in range(50):
+                call(osr, w, sets[i % len(sets)])
+                i += 1
+            torch.cuda.synchronize(device)
+
+    if sampler:
+        sampler.__enter__()
+    try:
+        sustain()  # same load, so the clock samples reflect the timed region
+        if torch.distributed.is_initialized():
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            call(osr, w, sets[i % len(sets)])
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+        elapsed_ms = start.elapsed_time(stop)
+        sustain()
+    finally:
+        if sampler:
+            sampler.__exit__(None, None, None)
+            clocks = sampler.summary()
+    del sets
+    torch.cuda.empty_cache()
+    return elapsed_ms, clocks
+
+
+def time_e2e(osr, w, steps, warmup, device):
+    """Same metric through the public API from pinned HOST buffers: every step
+    copies its inputs host->device, runs the call, and reads the outputs back."""
+    inp = workloads.make(w, seed=0, device="cpu")
+    host_in = {k: v.pin_memory() for k, v in inp.items()}
+    dev = {k: torch.empty_like(v, device=device) for k, v in inp.items()}
+    if w.op == "softmax":
+        dev["y"] = torch.empty(w.M, w.N, dtype=DT[w.out_dtype], device=device)
+    else:
+        dev["y"] = torch.empty_like(dev["x"])
+    outs = ["y"] + (["residual"] if w.op == "fused_add_rmsnorm" else [])
+    host_out = {k: torch.empty(dev[k].shape, dtype=dev[k].dtype, pin_memory=True) for k in outs}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in outs)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        for k, v in host_in.items():
+            dev[k].copy_(v, non_blocking=True)
+        call(osr, w, dev)
+        for k in outs:
+            host_out[k].copy_(dev[k], non_blocking=True)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(stop)
+    return {"value": round(w.min_bytes * steps / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / steps, 5),
+            "path": "pinned host -> cudaMemcpyAsync -> C ABI call -> cudaMemcpyAsync -> pinned host"}
+
+
+def copy_peak(osr, device, gib=2):
+    n = gib * (1 << 30)
+    a = torch.empty(n, dtype=torch.uint8, device=device)
+    b = torch.empty(n, dtype=torch.uint8, device=device)
+    a.fill_(1)
+    for _ in range(3):
+        osr.bench_copy(a, b)
+    torch.cuda.synchronize(device)
+    best = float("inf")
+    for _ in range(10):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        osr.bench_copy(a, b)
+        e.record()
+        torch.cuda.synchronize(device)
+        best = min(best, s.elapsed_time(e))
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * n / (best * 1e-3) / 1e9
+
+
+def cpu_baseline_for(w, budget_s=8.0):
+    """The oracle, as it stands (single thread), on a bounded sample of rows of
+    the same workload; value in the workload's GB/s (min bytes of the sample)."""
+    import oracle
+    oracle.set_threads(1)
+    rows = w.M
+    # estimate with a small probe, then size the sample to about budget_s
+    probe = max(1, min(rows, 4096 // max(1, w.N // 1024) or 1))
+    t = _oracle_time(oracle, w, probe)
+    per_row = max(t / probe, 1e-7)
+    sample = int(max(1, min(rows, budget_s / per_row)))
+    t = _oracle_time(oracle, w, sample)
+    frac = sample / w.M
+    gbs = w.min_bytes * frac / t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"{sample} of {w.M} rows of {w.name} (seed 0), fp64 C oracle, {t:.2f} s",
+            "seconds": round(t, 3)}
+
+
+def _oracle_inputs(w, rows):
+    """Oracle-format inputs (float32, or uint16 bf16 bits) for the first rows."""
+    if w.op == "softmax":
+        inp = workloads.softmax_inputs(rows, w.N, w.in_dtype, w.sigma, 0, w.shift, w.spikes_per_row,
+                                       w.spike, seed=0)
+    else:
+        inp = workloads.rmsnorm_inputs(rows, w.N, w.in_dtype, w.sigma, w.op == "fused_add_rmsnorm", seed=0)
+    out = {}
+    for k, v in inp.items():
+        v = v.contiguous()
+        out[k] = v.view(torch.int16).numpy().view(np.uint16) if v.dtype == torch.bfloat16 else v.numpy()
+    return out
+
+
+def _run_oracle(oracle, w, inp):
+    if w.op == "softmax":
+        y = oracle.softmax(inp["x"])
+        return oracle.round_to(y, w.out_dtype)
+    if w.op == "rmsnorm":
+        y = oracle.rmsnorm(inp["x"], inp["gamma"], w.eps)
+        return oracle.round_to(y, w.out_dtype)
+    h, y = oracle.fused_add_rmsnorm(inp["x"], inp["residual"], inp["gamma"], w.eps)
+    return oracle.round_to(h, w.out_dtype), oracle.round_to(y, w.out_dtype)
+
+
+def _oracle_time(oracle, w, rows):
+    inp = _oracle_inputs(w, rows)
+    t0 = time.perf_counter()
+    _run_oracle(oracle, w, inp)
+    return time.perf_counter() - t0
+
+
+def ours(args):
+    import online_softmax_row_gb300 as osr
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    peak, peak_src = measured_peaks()
+    w = workloads.WORKLOADS[args.workload]
+    osr.library()
+    plan = osr.plan_describe(OP_CODE[w.op], w.M, w.N, w.in_dtype, w.out_dtype, True,
+                             props.multi_processor_count)
+
+    elapsed_ms, clocks = time_workload(osr, w, args.steps, args.warmup, device, l2,
+                                       sampler_index=device.index, sustain_s=1.5)
+    max_ms, total_bytes = aggregate_over_ranks(elapsed_ms, w.min_bytes * args.steps, world)
+    value = total_bytes / (max_ms * 1e-3) / 1e9
+    per_launch_ms = elapsed_ms / args.steps / launches_per_call(plan, w.M)
+    achieved = w.min_bytes / launches_per_call(plan, w.M) / (per_launch_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.in_dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
+                   "out_dtype": w.out_dtype, "min_bytes_per_step": w.min_bytes, "kernel": plan,
+                   "l2": f"rotating {n_sets_for(w, l2)} input/output sets (> 2x L2 of traffic "
+                         f"between reuses); no flush", "parallelism": f"rows; {world} GPU(s), weak"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
+                     "peak_source": peak_src + " -- of measured" if "measured" in peak_src else peak_src,
+                     "algorithmic_bytes_per_launch": w.min_bytes // launches_per_call(plan, w.M)},
+        "gpu_launches": args.steps * launches_per_call(plan, w.M),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_suite:
+        result["peaks"] = {"nominal_gbs": NOMINAL_HBM_GBS, "driver_measured_gbs": peak,
+                           "copy_kernel_same_run_gbs": round(copy_peak(osr, device), 1)}
+        suite = []
+        for name, wl in workloads.WORKLOADS.items():
+            steps = max(10, min(200, int(2e9 * 20 / max(wl.min_bytes, 1) / 20)))
+            ms, _ = time_workload(osr, wl, steps, 5, device, l2)
+            p = osr.plan_describe(OP_CODE[wl.op], wl.M, wl.N, wl.in_dtype, wl.out_dtype, True,
+                                  props.multi_processor_count)
+            g = wl.min_bytes * steps / (ms * 1e-3) / 1e9
+            suite.append({"workload": name, "kernel": p, "min_bytes": wl.min_bytes,
+                          "us_per_call": round(ms / steps * 1e3, 3), "gbs": round(g, 1),
+                          "frac_measured": round(g / peak, 4), "frac_nominal": round(g / NOMINAL_HBM_GBS, 4),
+                          "frac_copy_same_run": round(g / result["peaks"]["copy_kernel_same_run_gbs"], 4),
+                          "launches_per_call": launches_per_call(p, wl.M)})
+        result["per_kernel"] = suite
+    if rank == 0:
+        result["e2e"] = time_e2e(osr, w, max(3, min(args.steps, 50)), args.warmup, device)
+        result["cpu_baseline"] = cpu_baseline_for(w)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    oracle.set_threads(1)
+    w = workloads.WORKLOADS[args.workload]
+    # each step: a bounded sample of rows of the same workload
+    rows = max(1, min(w.M, int(2_000_000 // max(w.N, 1))))
+    inp = _oracle_inputs(w, rows)
+    for _ in range(max(args.warmup, 0)):
+        _run_oracle(oracle, w, inp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _run_oracle(oracle, w, inp)
+    dt = time.perf_counter() - t0
+    sample_bytes = w.min_bytes * rows / w.M
+    value = sample_bytes * args.steps / dt / 1e9
+    sample = f"{rows} of {w.M} rows of {w.name} per step (seed 0), fp64 C oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
+                   "out_dtype": w.out_dtype, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.get_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--no-suite", action="store_true", help="skip the per-workload table")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

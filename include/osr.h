@@ -1,0 +1,154 @@
+/*
+ * osr.h -- C ABI of the GB300 (sm_103a) row-wise reduce-then-rescale library.
+ *
+ * Three operations, each applied independently to every row of a row-major
+ * matrix:
+ *
+ *   RMSNorm                y_j = x_j * (mean_j x_j^2 + eps)^(-1/2) * gamma_j
+ *   fused residual-add +   h = x + residual (written back to residual),
+ *     RMSNorm              out = RMSNorm(h) * gamma
+ *   safe softmax           y_i = exp(x_i - m) / d,  m = max_j x_j,
+ *                          d = sum_j exp(x_j - m), with (m, d) built by the
+ *                          online normaliser and its associative merge
+ *                          (m, d) = (max(m1, m2), d1 e^(m1-m) + d2 e^(m2-m)).
+ *
+ * Pages defining these operations (cited by title and section):
+ *   "RMSNorm、Softmax 与在线归约" (notes.kuangjux.top): "RMSNorm 归约什么",
+ *       "稳定 Softmax：归一化之前先减最大值", "Online Softmax 为什么要重缩放旧的和",
+ *       "从逐元素更新到合并两个 tile".
+ *   "GPU Kernel 工程（04）：共享内存与 reduction——softmax、LayerNorm 与 online
+ *       softmax" (arganzheng.life): 七 "softmax：safe、三遍、两遍、online",
+ *       八.1 "RMSNorm：均方在 FP32 累加", 八.3 "fused residual + RMSNorm".
+ *   "两个融合算子：RMSNorm 与 online softmax" (daleiyang.github.io): §5
+ *       "递推式怎么来的", "结合律：为什么能做树形归约".
+ *   "Softmax 与归一化", CUDA 进阶手册 (anrans.github.io): "Online softmax",
+ *       "按行长度选择并行方式" (row-length dispatch table).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named x, y, residual, gamma, out, row_max, row_sum are DEVICE
+ *   pointers (memory the current CUDA device can read/write: cudaMalloc,
+ *   cudaMallocAsync, managed memory, or a torch CUDA tensor's data_ptr()).
+ *   The caller owns every buffer; the library keeps no pointer after the
+ *   call returns.
+ * - Matrices are row-major and dense: row i starts at element i * (row
+ *   length).  Rows of length H (norms) or N (softmax).
+ * - Arithmetic is binary32 for every dtype (bfloat16 inputs are widened
+ *   exactly, sums and maxima accumulate in binary32); results are rounded
+ *   once to the output dtype, round-to-nearest-even.
+ * - Any alignment is accepted: 16-byte aligned buffers whose row length in
+ *   bytes is a multiple of 16 take 128-bit loads/stores, anything else takes
+ *   an element-wise path with the same arithmetic.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *   device work is enqueued on it asynchronously; no entry point
+ *   synchronises the device or the stream.  The split-row path draws a small
+ *   workspace (rows x pieces x 8 bytes) from the stream-ordered allocator
+ *   (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * - M == 0 is a no-op returning OSR_OK.  Row length <= 0, M < 0, a NULL
+ *   required pointer, or a dtype value outside osr_dtype return
+ *   OSR_ERR_INVALID before any device work.  Errors are reported only by
+ *   return value: nothing is printed and the process is never terminated.
+ * - Entry points are thread-safe; calls on the same stream execute in order.
+ */
+#ifndef OSR_H
+#define OSR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum osr_dtype {
+    OSR_F32 = 0,  /* IEEE binary32 */
+    OSR_BF16 = 1  /* bfloat16: the upper 16 bits of a binary32 */
+} osr_dtype;
+
+typedef enum osr_status {
+    OSR_OK = 0,
+    OSR_ERR_INVALID = 1,        /* bad size, NULL pointer or dtype value */
+    OSR_ERR_ALIGN = 2,          /* reserved: misalignment is never an error */
+    OSR_ERR_ALIAS = 3,          /* buffers overlap in a way the call forbids */
+    OSR_ERR_UNSUPPORTED = 4,    /* valid arguments outside what is implemented */
+    OSR_ERR_CUDA = 5,           /* a CUDA call or launch failed: osr_last_cuda_error() */
+    OSR_ERR_DEVICE_TIMEOUT = 6  /* reserved: no kernel of this library waits on a flag */
+} osr_status;
+
+/*
+ * RMSNorm forward: y[i, j] = x[i, j] * r_i * gamma[j],
+ * r_i = 1 / sqrt(sum_j x[i, j]^2 / H + eps).
+ *   x      [M, H] of dtype dt, read only (may equal y: in place)
+ *   gamma  [H] of dtype dt
+ *   eps    added to the mean square inside the square root
+ *   y      [M, H] of dtype dt, written
+ * y == x is allowed; any other overlap of y with x or gamma -> OSR_ERR_ALIAS.
+ */
+osr_status osr_rmsnorm_fwd(const void *x, const void *gamma, float eps, void *y,
+                           int64_t M, int64_t H, osr_dtype dt, void *stream);
+
+/*
+ * Fused residual-add + RMSNorm:
+ *   residual[i, j] <- round_dt(x[i, j] + residual[i, j])
+ *   out[i, j]      <- residual[i, j] * r_i * gamma[j]   (of the rounded sum)
+ *   x        [M, H] dtype dt, read only (may equal out: in place)
+ *   residual [M, H] dtype dt, read and overwritten
+ *   gamma    [H] dtype dt
+ *   out      [M, H] dtype dt, written
+ * out == x is allowed.  residual must not overlap x, out or gamma, and out
+ * must not overlap gamma -> otherwise OSR_ERR_ALIAS.
+ */
+osr_status osr_fused_add_rmsnorm(const void *x, void *residual, const void *gamma, float eps,
+                                 void *out, int64_t M, int64_t H, osr_dtype dt, void *stream);
+
+/*
+ * Row softmax: y[i, :] = softmax(x[i, :]).
+ *   x  [M, N] dtype in_dt, read only
+ *   y  [M, N] dtype out_dt, written
+ * Any in_dt/out_dt pair of OSR_F32/OSR_BF16.  y == x is allowed when
+ * in_dt == out_dt (in place); any other overlap -> OSR_ERR_ALIAS.
+ * Entries equal to -inf give 0; a row of only -inf gives NaN; a NaN or +inf
+ * entry makes its row NaN.
+ */
+osr_status osr_softmax_rows(const void *x, void *y, int64_t M, int64_t N,
+                            osr_dtype in_dt, osr_dtype out_dt, void *stream);
+
+/*
+ * Row softmax that also returns each row's normaliser statistics:
+ *   row_max [M] binary32: m_i = max_j x[i, j] (exact), may be NULL
+ *   row_sum [M] binary32: d_i = sum_j exp(x[i, j] - m_i), may be NULL
+ * so that log(sum_j exp(x[i, j])) = m_i + log(d_i).  Other arguments and
+ * rules as osr_softmax_rows; row_max/row_sum must not overlap x or y.
+ */
+osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float *row_sum,
+                                  int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
+                                  void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *osr_status_string(osr_status s);
+
+/* cudaError_t value recorded by the most recent OSR_ERR_CUDA on the calling
+ * thread (0 if none). */
+int osr_last_cuda_error(void);
+
+/*
+ * Which kernel the length-based dispatcher picks, without touching a GPU.
+ *   op        0 = RMSNorm, 1 = fused residual-add + RMSNorm, 2 = softmax
+ *   vec_ok    1 if every buffer is 16-byte aligned (the 128-bit path)
+ *   sm_count  streaming multiprocessors of the target device (152 on GB300)
+ *   buf       receives a NUL-terminated description, e.g.
+ *             "rows g=256 ept=16 vec" or "cluster cs=10 g=1024 ept=16 vec"
+ * Honours the OSR_FORCE_KERNEL environment variable exactly as the
+ * compute entry points do.  Returns OSR_ERR_INVALID on bad arguments.
+ */
+osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
+                             int vec_ok, int sm_count, char *buf, size_t buf_len);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int osr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSR_H */

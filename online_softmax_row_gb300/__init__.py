@@ -1,0 +1,201 @@
+"""GB300 (sm_103a) row-wise reduce-then-rescale: RMSNorm, fused residual-add
++ RMSNorm, and safe softmax by the online (m, d) normaliser.
+
+Thin ctypes binding over the C ABI in ``include/osr.h`` (libosr.so, built
+in-tree by ``online_softmax_row_gb300.build``).  This module only marshals
+torch CUDA tensors (pointers, sizes, dtype codes, the current stream); every
+step of the computation runs in the library's CUDA kernels.  There is no
+fallback: if the library is not built, or an argument is rejected, a call
+raises ``OsrError``.
+
+Python name          C entry point
+rmsnorm_fwd          osr_rmsnorm_fwd
+fused_add_rmsnorm    osr_fused_add_rmsnorm
+softmax_rows         osr_softmax_rows
+softmax_rows_stats   osr_softmax_rows_stats
+plan_describe        osr_plan_describe
+bench_copy           osr_bench_copy
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = ["OsrError", "rmsnorm_fwd", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
+           "plan_describe", "bench_copy", "library", "library_path", "OP_RMSNORM", "OP_FUSED",
+           "OP_SOFTMAX"]
+
+OP_RMSNORM, OP_FUSED, OP_SOFTMAX = 0, 1, 2
+_DT = {torch.float32: 0, torch.bfloat16: 1}
+_DT_NAME = {"f32": 0, "bf16": 1}
+_STATUS = {0: "OSR_OK", 1: "OSR_ERR_INVALID", 2: "OSR_ERR_ALIGN", 3: "OSR_ERR_ALIAS",
+           4: "OSR_ERR_UNSUPPORTED", 5: "OSR_ERR_CUDA", 6: "OSR_ERR_DEVICE_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class OsrError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        self.name = _STATUS.get(status, str(status))
+        super().__init__(f"{where}: {self.name}{': ' + detail if detail else ''}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def library():
+    """The loaded libosr.so (ctypes.CDLL).  Raises OsrError if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise OsrError(1, "libosr.so", f"not built at {path}; run "
+                           "`python -m online_softmax_row_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lib.osr_rmsnorm_fwd.argtypes = [P, P, F, P, I64, I64, I, P]
+        lib.osr_fused_add_rmsnorm.argtypes = [P, P, P, F, P, I64, I64, I, P]
+        lib.osr_softmax_rows.argtypes = [P, P, I64, I64, I, I, P]
+        lib.osr_softmax_rows_stats.argtypes = [P, P, P, P, I64, I64, I, I, P]
+        lib.osr_status_string.argtypes = [I]
+        lib.osr_status_string.restype = ctypes.c_char_p
+        lib.osr_last_cuda_error.restype = I
+        lib.osr_plan_describe.argtypes = [I, I64, I64, I, I, I, I, ctypes.c_char_p, ctypes.c_size_t]
+        lib.osr_version.restype = I
+        lib.osr_bench_copy.argtypes = [P, P, ctypes.c_size_t, P]
+        for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
+                   "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy"):
+            getattr(lib, fn).restype = I
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        lib = library()
+        detail = lib.osr_status_string(status).decode()
+        if status == 5:
+            detail += f" (cudaError {lib.osr_last_cuda_error()})"
+        raise OsrError(status, where, detail)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _rows(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise OsrError(1, name, "expected a CUDA tensor")
+    if t.dtype not in _DT:
+        raise OsrError(1, name, f"dtype {t.dtype} (float32 or bfloat16 expected)")
+    if not t.is_contiguous():
+        raise OsrError(1, name, "expected a contiguous (row-major) tensor")
+    if t.dim() == 0:
+        raise OsrError(1, name, "expected at least one dimension")
+    n = t.shape[-1]
+    m = t.numel() // n if n else 0
+    return m, n
+
+
+def rmsnorm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x * rsqrt(mean(x^2, -1) + eps) * gamma over the last dimension."""
+    M, H = _rows(x, "x")
+    if gamma.shape != (H,) or gamma.dtype != x.dtype:
+        raise OsrError(1, "gamma", f"expected shape ({H},) and dtype {x.dtype}")
+    _rows(gamma, "gamma")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype:
+        raise OsrError(1, "out", "shape/dtype must match x")
+    _rows(out, "out")
+    with torch.cuda.device(x.device):
+        _check(library().osr_rmsnorm_fwd(x.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
+                                         M, H, _DT[x.dtype], _stream(x)), "osr_rmsnorm_fwd")
+    return out
+
+
+def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor,
+                      eps: float = 1e-6, out: torch.Tensor | None = None) -> torch.Tensor:
+    """residual <- x + residual (in place); returns RMSNorm(residual) * gamma."""
+    M, H = _rows(x, "x")
+    if residual.shape != x.shape or residual.dtype != x.dtype:
+        raise OsrError(1, "residual", "shape/dtype must match x")
+    _rows(residual, "residual")
+    if gamma.shape != (H,) or gamma.dtype != x.dtype:
+        raise OsrError(1, "gamma", f"expected shape ({H},) and dtype {x.dtype}")
+    _rows(gamma, "gamma")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype:
+        raise OsrError(1, "out", "shape/dtype must match x")
+    _rows(out, "out")
+    with torch.cuda.device(x.device):
+        _check(library().osr_fused_add_rmsnorm(x.data_ptr(), residual.data_ptr(), gamma.data_ptr(),
+                                               float(eps), out.data_ptr(), M, H, _DT[x.dtype],
+                                               _stream(x)), "osr_fused_add_rmsnorm")
+    return out
+
+
+def _softmax_out(x, out, out_dtype):
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    elif out.shape != x.shape or (out_dtype is not None and out.dtype != out_dtype):
+        raise OsrError(1, "out", "shape must match x (and dtype out_dtype)")
+    _rows(out, "out")
+    return out
+
+
+def softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None,
+                 out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """Softmax over the last dimension (float32 or bfloat16 in and out)."""
+    M, N = _rows(x, "x")
+    out = _softmax_out(x, out, out_dtype)
+    with torch.cuda.device(x.device):
+        _check(library().osr_softmax_rows(x.data_ptr(), out.data_ptr(), M, N, _DT[x.dtype],
+                                          _DT[out.dtype], _stream(x)), "osr_softmax_rows")
+    return out
+
+
+def softmax_rows_stats(x: torch.Tensor, out: torch.Tensor | None = None,
+                       out_dtype: torch.dtype | None = None):
+    """Softmax plus each row's (max, sum of exp(x - max)) as float32 tensors."""
+    M, N = _rows(x, "x")
+    out = _softmax_out(x, out, out_dtype)
+    lead = x.shape[:-1]
+    row_max = torch.empty(lead, dtype=torch.float32, device=x.device)
+    row_sum = torch.empty(lead, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(library().osr_softmax_rows_stats(x.data_ptr(), out.data_ptr(), row_max.data_ptr(),
+                                                row_sum.data_ptr(), M, N, _DT[x.dtype],
+                                                _DT[out.dtype], _stream(x)), "osr_softmax_rows_stats")
+    return out, row_max, row_sum
+
+
+def plan_describe(op: int, M: int, N: int, in_dtype: str = "f32", out_dtype: str | None = None,
+                  vec_ok: bool = True, sm_count: int = 152) -> str:
+    """Kernel the dispatcher picks for a shape (host-only, no GPU needed)."""
+    buf = ctypes.create_string_buffer(128)
+    _check(library().osr_plan_describe(op, M, N, _DT_NAME[in_dtype], _DT_NAME[out_dtype or in_dtype],
+                                       int(vec_ok), sm_count, buf, 128), "osr_plan_describe")
+    return buf.value.decode()
+
+
+def bench_copy(src: torch.Tensor, dst: torch.Tensor) -> None:
+    """dst <- src bytes with the library's 128-bit copy kernel (HBM peak probe)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise OsrError(1, "bench_copy", "sizes differ")
+    with torch.cuda.device(src.device):
+        _check(library().osr_bench_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream(src)),
+               "osr_bench_copy")

@@ -1,0 +1,170 @@
+// device_common.cuh -- storage types, 16-byte vector I/O and cluster /
+// distributed-shared-memory primitives for sm_103a.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <float.h>
+#include <stdint.h>
+
+namespace osr {
+
+enum class Dt : int { F32 = 0, BF16 = 1 };
+
+template <Dt D>
+struct Elem;
+template <>
+struct Elem<Dt::F32> {
+    static constexpr int kBytes = 4;
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+};
+template <>
+struct Elem<Dt::BF16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kVec = 8;
+};
+
+// ---------------------------------------------------------------- conversions
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// two floats -> two bfloat16 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ float round_bf16(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+template <Dt D>
+__device__ __forceinline__ float round_to(float v) {
+    if constexpr (D == Dt::BF16) return round_bf16(v);
+    return v;
+}
+
+// ---------------------------------------------------------------- loads
+// A "unit" is U consecutive elements: one 16-byte vector (U = kVec) or one
+// scalar (U = 1).  `e` is the element offset of the unit from `base`.
+// Streaming inputs are read with the evict-first (.cs) hint: each byte is
+// read once, so it should not push reusable lines out of L2.
+
+// Stream   : read once (ld.global.cs, evict-first);
+// Keep     : default caching, for data read again soon (split-row pass 1);
+// ReadOnly : never written during the kernel and shared by many CTAs
+//            (gamma), through the non-coherent read-only path.
+enum class Hint : int { Stream = 0, Keep = 1, ReadOnly = 2 };
+
+template <Hint H>
+__device__ __forceinline__ uint4 ld16(const void *p) {
+    if constexpr (H == Hint::Stream)
+        return __ldcs(reinterpret_cast<const uint4 *>(p));
+    else if constexpr (H == Hint::ReadOnly)
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    else
+        return *reinterpret_cast<const uint4 *>(p);
+}
+
+template <Dt D, int U, Hint H = Hint::Stream>
+__device__ __forceinline__ void load_unit(const void *base, int64_t e, float (&v)[U]) {
+    if constexpr (U == 1) {
+        if constexpr (D == Dt::F32) {
+            v[0] = reinterpret_cast<const float *>(base)[e];
+        } else {
+            const uint16_t b = reinterpret_cast<const uint16_t *>(base)[e];
+            v[0] = __uint_as_float(uint32_t(b) << 16);
+        }
+    } else {
+        static_assert(U == Elem<D>::kVec, "a vector unit is 16 bytes");
+        const uint4 q = ld16<H>(reinterpret_cast<const char *>(base) + e * Elem<D>::kBytes);
+        if constexpr (D == Dt::F32) {
+            v[0] = __uint_as_float(q.x);
+            v[1] = __uint_as_float(q.y);
+            v[2] = __uint_as_float(q.z);
+            v[3] = __uint_as_float(q.w);
+        } else {
+            v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x);
+            v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+            v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z);
+            v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- stores
+// U elements of dtype D from binary32 values, rounded to nearest even.
+// U = 1: one scalar; U = 4 or 8: 8..32 bytes as 16-byte (or, for 4 bfloat16,
+// 8-byte) vector stores.  Outputs are written with the streaming (.cs) hint.
+
+template <Dt D, int U>
+__device__ __forceinline__ void store_unit(void *base, int64_t e, const float (&v)[U]) {
+    if constexpr (U == 1) {
+        if constexpr (D == Dt::F32)
+            reinterpret_cast<float *>(base)[e] = v[0];
+        else
+            reinterpret_cast<__nv_bfloat16 *>(base)[e] = __float2bfloat16_rn(v[0]);
+    } else if constexpr (D == Dt::F32) {
+        static_assert(U % 4 == 0, "f32 vector stores cover 4 elements");
+        float4 *p = reinterpret_cast<float4 *>(reinterpret_cast<float *>(base) + e);
+#pragma unroll
+        for (int k = 0; k < U / 4; ++k)
+            __stcs(p + k, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+    } else {
+        static_assert(U == 4 || U == 8, "bf16 vector stores cover 4 or 8 elements");
+        char *p = reinterpret_cast<char *>(base) + e * 2;
+        if constexpr (U == 8) {
+            uint4 q;
+            q.x = pack_bf16x2(v[0], v[1]);
+            q.y = pack_bf16x2(v[2], v[3]);
+            q.z = pack_bf16x2(v[4], v[5]);
+            q.w = pack_bf16x2(v[6], v[7]);
+            __stcs(reinterpret_cast<uint4 *>(p), q);
+        } else {
+            uint2 q;
+            q.x = pack_bf16x2(v[0], v[1]);
+            q.y = pack_bf16x2(v[2], v[3]);
+            __stcs(reinterpret_cast<uint2 *>(p), q);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- clusters
+// Thread-block cluster barrier (split arrive / wait) and distributed shared
+// memory access, as PTX.  Every thread of every CTA of the cluster executes
+// each arrive and each wait exactly once per phase (.aligned).
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// address of the same shared variable in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+}  // namespace osr

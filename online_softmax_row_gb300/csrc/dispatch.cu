@@ -1,0 +1,495 @@
+// dispatch.cu -- the C ABI (include/osr.h): argument validation, the
+// length-based dispatcher, and execution of a plan on the caller's stream.
+//
+// Dispatch follows the row-length table of "Softmax 与归一化"
+// (anrans.github.io), "按行长度选择并行方式": short rows -> several rows per
+// warp; up to about a thousand elements -> one warp per row; thousands ->
+// one block per row; rows longer than one block's registers -> several
+// blocks per row.  Here the last step has two forms: a thread-block cluster
+// whose CTAs exchange their partial statistics through distributed shared
+// memory (row still read once), and, beyond what a cluster can hold, two
+// passes through a small global workspace.
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <stdio.h>
+#include <tuple>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/osr.h"
+#include "launch.h"
+
+namespace osr {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+osr_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return OSR_ERR_CUDA;
+}
+
+constexpr int kL2BudgetBytes = 48 << 20;  // re-read set of one split batch
+
+int elem_bytes(osr_dtype d) { return d == OSR_F32 ? 4 : 2; }
+int vec_elems(osr_dtype d) { return d == OSR_F32 ? 4 : 8; }
+bool dtype_ok(osr_dtype d) { return d == OSR_F32 || d == OSR_BF16; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int pow2ceil(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// ------------------------------------------------------------ device facts
+struct DeviceInfo {
+    int sms = 0;
+    int max_cluster = 8;
+};
+
+osr_status device_info(DeviceInfo *out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return OSR_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DeviceInfo d;
+        int major = 0, cluster = 0;
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&cluster, cudaDevAttrClusterLaunch, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        d.max_cluster = cluster ? (major >= 10 ? 16 : 8) : 1;
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = cache[dev];
+    return OSR_OK;
+}
+
+// ------------------------------------------------------------ planning
+// Units: a unit is one 16-byte input vector on the vector path, else one
+// element; each thread holds kEpt elements (kEpt / u units) per tile.
+
+// Value of `key` in "tier:key=v,key=v"; keys match whole tokens only.
+bool parse_kv(const char *s, const char *key, int64_t *v) {
+    const size_t n = strlen(key);
+    for (const char *p = strchr(s, ':'); p && *p; p = strchr(p + 1, ',')) {
+        const char *k = p + 1;
+        if (strncmp(k, key, n) == 0 && k[n] == '=') {
+            char *end = nullptr;
+            long long x = strtoll(k + n + 1, &end, 10);
+            if (end == k + n + 1) return false;
+            *v = x;
+            return true;
+        }
+    }
+    return false;
+}
+
+void split_shape(int64_t M, int64_t N, int64_t nunits, int upt, int in_bytes, int sms,
+                 int64_t force_s, int64_t force_b, Plan *p) {
+    const int64_t row_bytes = N * in_bytes;
+    int64_t b = force_b > 0 ? force_b : kL2BudgetBytes / (row_bytes > 0 ? row_bytes : 1);
+    if (b < 1) b = 1;
+    if (b > M) b = M;
+    int64_t s = force_s;
+    if (s <= 0) {
+        s = cdiv(2 * (int64_t)sms, b);
+        const int64_t most = cdiv(nunits, (int64_t)kSplitThreads * upt);  // >= one full tile
+        if (s > most) s = most;
+    }
+    if (s > kMaxPieces) s = kMaxPieces;
+    if (s > nunits) s = nunits;
+    if (s < 1) s = 1;
+    p->tier = Tier::Split;
+    p->g = kSplitThreads;
+    p->cs = (int)s;
+    p->chunk = cdiv(nunits, s);
+    p->batch_rows = b;
+}
+
+osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt, bool vec,
+                     int sms, int max_cluster, Plan *p) {
+    (void)op;
+    (void)out_dt;
+    *p = Plan();
+    p->vec = vec;
+    p->u = vec ? vec_elems(in_dt) : 1;
+    const int upt = kEpt / p->u;
+    const int64_t nunits = vec ? N / p->u : N;
+    const int in_bytes = elem_bytes(in_dt);
+
+    const char *force = getenv("OSR_FORCE_KERNEL");
+    if (force && *force) {
+        p->forced = true;
+        int64_t g = 0, cs = 0, s = 0, b = 0;
+        if (strncmp(force, "rows", 4) == 0) {
+            if (!parse_kv(force, "g", &g)) return OSR_ERR_UNSUPPORTED;
+            if (g < 1 || g > 1024 || (g & (g - 1)) || g * upt < nunits) return OSR_ERR_UNSUPPORTED;
+            p->tier = Tier::Rows;
+            p->g = (int)g;
+            return OSR_OK;
+        }
+        if (strncmp(force, "cluster", 7) == 0) {
+            if (!parse_kv(force, "g", &g)) g = 1024;
+            if (!parse_kv(force, "cs", &cs)) cs = cdiv(nunits, g * upt);
+            if ((g != 256 && g != 1024) || cs < 1 || cs > max_cluster || cs * g * upt < nunits)
+                return OSR_ERR_UNSUPPORTED;
+            p->tier = Tier::Cluster;
+            p->g = (int)g;
+            p->cs = (int)cs;
+            p->chunk = cdiv(nunits, cs);
+            if (p->chunk > g * upt) return OSR_ERR_UNSUPPORTED;
+            return OSR_OK;
+        }
+        if (strncmp(force, "split", 5) == 0) {
+            parse_kv(force, "s", &s);
+            parse_kv(force, "b", &b);
+            if (s > kMaxPieces) return OSR_ERR_UNSUPPORTED;
+            split_shape(M, N, nunits, upt, in_bytes, sms, s, b, p);
+            return OSR_OK;
+        }
+        return OSR_ERR_UNSUPPORTED;
+    }
+
+    // 1. the whole row in one group or CTA, register-cached
+    const int g = pow2ceil(cdiv(nunits, upt));
+    if (g <= 1024) {
+        p->tier = Tier::Rows;
+        p->g = g;
+        return OSR_OK;
+    }
+    // 2. a cluster of 1024-thread CTAs, still register-cached (one read)
+    const int64_t cs = cdiv(nunits, (int64_t)1024 * upt);
+    if (cs <= max_cluster) {
+        p->tier = Tier::Cluster;
+        p->g = 1024;
+        p->cs = (int)cs;
+        p->chunk = cdiv(nunits, cs);
+        return OSR_OK;
+    }
+    // 3. two passes through a workspace
+    split_shape(M, N, nunits, upt, in_bytes, sms, 0, 0, p);
+    return OSR_OK;
+}
+
+void describe(const Plan &p, char *buf, size_t n) {
+    const char *v = p.vec ? "vec" : "scalar";
+    switch (p.tier) {
+    case Tier::Rows:
+        snprintf(buf, n, "rows g=%d ept=%d %s", p.g, kEpt, v);
+        break;
+    case Tier::Cluster:
+        snprintf(buf, n, "cluster cs=%d g=%d ept=%d %s", p.cs, p.g, kEpt, v);
+        break;
+    case Tier::Split:
+        snprintf(buf, n, "split s=%d b=%lld g=%d ept=%d %s", p.cs, (long long)p.batch_rows, p.g,
+                 kEpt, v);
+        break;
+    }
+}
+
+// ------------------------------------------------------------ execution
+
+cudaError_t launch(Op op, osr_dtype in_dt, osr_dtype out_dt, Kind k, const RowArgs &a,
+                   const Plan &p, int64_t grid, cudaStream_t st) {
+    if (op == Op::Softmax) {
+        if (in_dt == OSR_F32 && out_dt == OSR_F32)
+            return launch_softmax<Dt::F32, Dt::F32>(k, a, p.g, p.vec, grid, st);
+        if (in_dt == OSR_F32 && out_dt == OSR_BF16)
+            return launch_softmax<Dt::F32, Dt::BF16>(k, a, p.g, p.vec, grid, st);
+        if (in_dt == OSR_BF16 && out_dt == OSR_F32)
+            return launch_softmax<Dt::BF16, Dt::F32>(k, a, p.g, p.vec, grid, st);
+        return launch_softmax<Dt::BF16, Dt::BF16>(k, a, p.g, p.vec, grid, st);
+    }
+    const bool fused = op == Op::FusedAddRmsNorm;
+    if (in_dt == OSR_F32)
+        return fused ? launch_rmsnorm<Dt::F32, true>(k, a, p.g, p.vec, grid, st)
+                     : launch_rmsnorm<Dt::F32, false>(k, a, p.g, p.vec, grid, st);
+    return fused ? launch_rmsnorm<Dt::BF16, true>(k, a, p.g, p.vec, grid, st)
+                 : launch_rmsnorm<Dt::BF16, false>(k, a, p.g, p.vec, grid, st);
+}
+
+cudaError_t cluster_occupancy(Op op, osr_dtype in_dt, osr_dtype out_dt, const Plan &p, int *n) {
+    if (op == Op::Softmax) {
+        if (in_dt == OSR_F32 && out_dt == OSR_F32)
+            return softmax_cluster_occupancy<Dt::F32, Dt::F32>(p.g, p.vec, p.cs, n);
+        if (in_dt == OSR_F32 && out_dt == OSR_BF16)
+            return softmax_cluster_occupancy<Dt::F32, Dt::BF16>(p.g, p.vec, p.cs, n);
+        if (in_dt == OSR_BF16 && out_dt == OSR_F32)
+            return softmax_cluster_occupancy<Dt::BF16, Dt::F32>(p.g, p.vec, p.cs, n);
+        return softmax_cluster_occupancy<Dt::BF16, Dt::BF16>(p.g, p.vec, p.cs, n);
+    }
+    const bool fused = op == Op::FusedAddRmsNorm;
+    if (in_dt == OSR_F32)
+        return fused ? rmsnorm_cluster_occupancy<Dt::F32, true>(p.g, p.vec, p.cs, n)
+                     : rmsnorm_cluster_occupancy<Dt::F32, false>(p.g, p.vec, p.cs, n);
+    return fused ? rmsnorm_cluster_occupancy<Dt::BF16, true>(p.g, p.vec, p.cs, n)
+                 : rmsnorm_cluster_occupancy<Dt::BF16, false>(p.g, p.vec, p.cs, n);
+}
+
+// A cluster plan whose cluster shape the device cannot schedule becomes a
+// split plan (or, if it was forced, an OSR_ERR_UNSUPPORTED).  Results of the
+// occupancy query are cached per device and kernel shape.
+osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
+                              const DeviceInfo &di, Plan *p) {
+    if (p->tier != Tier::Cluster) return OSR_OK;
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int, int, int>, int> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const auto key = std::make_tuple(dev, (int)op, (int)in_dt, (int)out_dt, p->g, (int)p->vec, p->cs);
+    int n = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) n = it->second;
+    }
+    if (n < 0) {
+        e = cluster_occupancy(op, in_dt, out_dt, *p, &n);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        std::lock_guard<std::mutex> lock(mu);
+        cache[key] = n;
+    }
+    if (n > 0) return OSR_OK;
+    if (p->forced) return OSR_ERR_UNSUPPORTED;
+    const int upt = kEpt / p->u;
+    const int64_t nunits = p->vec ? N / p->u : N;
+    split_shape(M, N, nunits, upt, elem_bytes(in_dt), di.sms, 0, 0, p);
+    return OSR_OK;
+}
+
+osr_status execute(Op op, osr_dtype in_dt, osr_dtype out_dt, RowArgs a, const Plan &p,
+                   cudaStream_t st) {
+    const int64_t M = a.M;
+    cudaError_t e = cudaSuccess;
+    switch (p.tier) {
+    case Tier::Rows: {
+        const int64_t grid = p.g <= 32 ? cdiv(M, 128 / p.g) : M;
+        if (grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
+        e = launch(op, in_dt, out_dt, Kind::Rows, a, p, grid, st);
+        break;
+    }
+    case Tier::Cluster: {
+        const int64_t grid = M * p.cs;
+        if (grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
+        a.cs = p.cs;
+        a.chunk = p.chunk;
+        e = launch(op, in_dt, out_dt, Kind::Cluster, a, p, grid, st);
+        break;
+    }
+    case Tier::Split: {
+        a.cs = p.cs;
+        a.chunk = p.chunk;
+        const size_t state = op == Op::Softmax ? sizeof(float2) : sizeof(float);
+        void *ws = nullptr;
+        if ((e = cudaMallocAsync(&ws, (size_t)M * p.cs * state, st)) != cudaSuccess)
+            return cuda_fail(e);
+        a.ws = ws;
+        for (int64_t r0 = 0; r0 < M && e == cudaSuccess; r0 += p.batch_rows) {
+            const int64_t rows = M - r0 < p.batch_rows ? M - r0 : p.batch_rows;
+            const int64_t grid = rows * p.cs;
+            if (grid > 0x7fffffffLL) {
+                e = cudaErrorInvalidConfiguration;
+                break;
+            }
+            a.row0 = r0;
+            e = launch(op, in_dt, out_dt, Kind::SplitStats, a, p, grid, st);
+            if (e == cudaSuccess) e = launch(op, in_dt, out_dt, Kind::SplitApply, a, p, grid, st);
+        }
+        cudaError_t f = cudaFreeAsync(ws, st);
+        if (e == cudaSuccess) e = f;
+        break;
+    }
+    }
+    return e == cudaSuccess ? OSR_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------ validation
+
+bool overlaps(const void *a, int64_t an, const void *b, int64_t bn) {
+    const char *pa = (const char *)a, *pb = (const char *)b;
+    return pa < pb + bn && pb < pa + an;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// The buffer must be memory the device can address: device, managed, or
+// (on systems with unified addressing of host memory) registered-mapped host
+// memory is reported by the runtime; plain unregistered host memory is not.
+bool device_accessible(const void *p) {
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+osr_status check_sizes(int64_t M, int64_t N) {
+    if (M < 0 || N <= 0) return OSR_ERR_INVALID;
+    if (N > ((int64_t)1 << 40) || M > ((int64_t)1 << 40)) return OSR_ERR_UNSUPPORTED;
+    return OSR_OK;
+}
+
+}  // namespace
+}  // namespace osr
+
+using namespace osr;
+
+extern "C" {
+
+const char *osr_status_string(osr_status s) {
+    switch (s) {
+    case OSR_OK: return "ok";
+    case OSR_ERR_INVALID: return "invalid argument (size, null pointer or dtype)";
+    case OSR_ERR_ALIGN: return "misaligned buffer";
+    case OSR_ERR_ALIAS: return "buffers overlap in a way the call forbids";
+    case OSR_ERR_UNSUPPORTED: return "arguments outside what is implemented";
+    case OSR_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case OSR_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int osr_last_cuda_error(void) { return g_last_cuda_error; }
+
+int osr_version(void) { return 100; }
+
+osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
+                             int vec_ok, int sm_count, char *buf, size_t buf_len) {
+    if (op < 0 || op > 2 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
+        sm_count <= 0)
+        return OSR_ERR_INVALID;
+    if (op != 2 && in_dt != out_dt) return OSR_ERR_UNSUPPORTED;
+    osr_status s = check_sizes(M, N);
+    if (s != OSR_OK) return s;
+    const bool vec = vec_ok && (N % vec_elems(in_dt)) == 0;
+    Plan p;
+    s = make_plan((Op)op, M, N, in_dt, out_dt, vec, sm_count, 16, &p);
+    if (s != OSR_OK) return s;
+    describe(p, buf, buf_len);
+    return OSR_OK;
+}
+
+osr_status osr_rmsnorm_fwd(const void *x, const void *gamma, float eps, void *y, int64_t M,
+                           int64_t H, osr_dtype dt, void *stream) {
+    osr_status s = check_sizes(M, H);
+    if (s != OSR_OK) return s;
+    if (!dtype_ok(dt)) return OSR_ERR_INVALID;
+    if (M == 0) return OSR_OK;
+    if (!x || !gamma || !y) return OSR_ERR_INVALID;
+    const int64_t bytes = M * H * elem_bytes(dt), gbytes = H * elem_bytes(dt);
+    if ((y != x && overlaps(x, bytes, y, bytes)) || overlaps(y, bytes, gamma, gbytes))
+        return OSR_ERR_ALIAS;
+    if (!device_accessible(x) || !device_accessible(gamma) || !device_accessible(y))
+        return OSR_ERR_INVALID;
+    DeviceInfo di;
+    if ((s = device_info(&di)) != OSR_OK) return s;
+    const bool vec = aligned16(x) && aligned16(gamma) && aligned16(y) && H % vec_elems(dt) == 0;
+    Plan p;
+    if ((s = make_plan(Op::RmsNorm, M, H, dt, dt, vec, di.sms, di.max_cluster, &p)) != OSR_OK)
+        return s;
+    if ((s = check_cluster_plan(Op::RmsNorm, M, H, dt, dt, di, &p)) != OSR_OK) return s;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.y = y;
+    a.M = M;
+    a.N = H;
+    a.eps = eps;
+    return execute(Op::RmsNorm, dt, dt, a, p, (cudaStream_t)stream);
+}
+
+osr_status osr_fused_add_rmsnorm(const void *x, void *residual, const void *gamma, float eps,
+                                 void *out, int64_t M, int64_t H, osr_dtype dt, void *stream) {
+    osr_status s = check_sizes(M, H);
+    if (s != OSR_OK) return s;
+    if (!dtype_ok(dt)) return OSR_ERR_INVALID;
+    if (M == 0) return OSR_OK;
+    if (!x || !residual || !gamma || !out) return OSR_ERR_INVALID;
+    const int64_t bytes = M * H * elem_bytes(dt), gbytes = H * elem_bytes(dt);
+    if (overlaps(residual, bytes, x, bytes) || overlaps(residual, bytes, out, bytes) ||
+        overlaps(residual, bytes, gamma, gbytes) || overlaps(out, bytes, gamma, gbytes) ||
+        (out != x && overlaps(out, bytes, x, bytes)))
+        return OSR_ERR_ALIAS;
+    if (!device_accessible(x) || !device_accessible(residual) || !device_accessible(gamma) ||
+        !device_accessible(out))
+        return OSR_ERR_INVALID;
+    DeviceInfo di;
+    if ((s = device_info(&di)) != OSR_OK) return s;
+    const bool vec = aligned16(x) && aligned16(residual) && aligned16(gamma) && aligned16(out) &&
+                     H % vec_elems(dt) == 0;
+    Plan p;
+    if ((s = make_plan(Op::FusedAddRmsNorm, M, H, dt, dt, vec, di.sms, di.max_cluster, &p)) !=
+        OSR_OK)
+        return s;
+    if ((s = check_cluster_plan(Op::FusedAddRmsNorm, M, H, dt, dt, di, &p)) != OSR_OK) return s;
+    RowArgs a = {};
+    a.x = x;
+    a.res = residual;
+    a.gamma = gamma;
+    a.y = out;
+    a.M = M;
+    a.N = H;
+    a.eps = eps;
+    return execute(Op::FusedAddRmsNorm, dt, dt, a, p, (cudaStream_t)stream);
+}
+
+osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float *row_sum,
+                                  int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
+                                  void *stream) {
+    osr_status s = check_sizes(M, N);
+    if (s != OSR_OK) return s;
+    if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return OSR_ERR_INVALID;
+    if (M == 0) return OSR_OK;
+    if (!x || !y) return OSR_ERR_INVALID;
+    const int64_t xb = M * N * elem_bytes(in_dt), yb = M * N * elem_bytes(out_dt);
+    const bool in_place = x == y && in_dt == out_dt;
+    if (!in_place && overlaps(x, xb, y, yb)) return OSR_ERR_ALIAS;
+    const void *stats[2] = {row_max, row_sum};
+    for (const void *q : stats)
+        if (q && (overlaps(q, M * 4, x, xb) || overlaps(q, M * 4, y, yb))) return OSR_ERR_ALIAS;
+    if (row_max && row_sum && overlaps(row_max, M * 4, row_sum, M * 4)) return OSR_ERR_ALIAS;
+    if (!device_accessible(x) || !device_accessible(y)) return OSR_ERR_INVALID;
+    if ((row_max && !device_accessible(row_max)) || (row_sum && !device_accessible(row_sum)))
+        return OSR_ERR_INVALID;
+    DeviceInfo di;
+    if ((s = device_info(&di)) != OSR_OK) return s;
+    const bool vec = aligned16(x) && aligned16(y) && N % vec_elems(in_dt) == 0;
+    Plan p;
+    if ((s = make_plan(Op::Softmax, M, N, in_dt, out_dt, vec, di.sms, di.max_cluster, &p)) !=
+        OSR_OK)
+        return s;
+    if ((s = check_cluster_plan(Op::Softmax, M, N, in_dt, out_dt, di, &p)) != OSR_OK) return s;
+    RowArgs a = {};
+    a.x = x;
+    a.y = y;
+    a.row_max = row_max;
+    a.row_sum = row_sum;
+    a.M = M;
+    a.N = N;
+    return execute(Op::Softmax, in_dt, out_dt, a, p, (cudaStream_t)stream);
+}
+
+osr_status osr_softmax_rows(const void *x, void *y, int64_t M, int64_t N, osr_dtype in_dt,
+                            osr_dtype out_dt, void *stream) {
+    return osr_softmax_rows_stats(x, y, nullptr, nullptr, M, N, in_dt, out_dt, stream);
+}
+
+}  // extern "C"

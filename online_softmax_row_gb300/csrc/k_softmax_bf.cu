@@ -1,0 +1,8 @@
+// Softmax kernels, input BF16 / output F32.
+#include "launch_impl.cuh"
+
+namespace osr {
+template cudaError_t launch_softmax<Dt::BF16, Dt::F32>(Kind, const RowArgs &, int, bool, int64_t,
+                                                    cudaStream_t);
+template cudaError_t softmax_cluster_occupancy<Dt::BF16, Dt::F32>(int, bool, int, int *);
+}  // namespace osr

@@ -1,0 +1,53 @@
+// launch.h -- host-side plan and launcher declarations shared by the
+// dispatcher (dispatch.cu) and the per-dtype kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rows.cuh"
+
+namespace osr {
+
+enum class Op : int { RmsNorm = 0, FusedAddRmsNorm = 1, Softmax = 2 };
+
+// Rows    : register-cached, one group / CTA per row        (one launch)
+// Cluster : register-cached, a CTA cluster per row (DSMEM)  (one launch)
+// Split   : S CTAs per row, partials in a workspace         (two launches)
+enum class Tier : int { Rows = 0, Cluster = 1, Split = 2 };
+
+// Which kernel of a tier a launch runs.
+enum class Kind : int { Rows = 0, Cluster = 1, SplitStats = 2, SplitApply = 3 };
+
+constexpr int kEpt = 16;           // elements per thread per tile
+constexpr int kSplitThreads = 512;  // threads per split-row CTA
+constexpr int kMaxPieces = kSplitThreads;
+
+struct Plan {
+    Tier tier = Tier::Rows;
+    int g = 1;               // threads per row (Rows) or per CTA (Cluster, Split)
+    int cs = 1;              // Cluster: CTAs per row; Split: pieces per row
+    int64_t chunk = 0;       // Cluster / Split: units per CTA piece
+    int64_t batch_rows = 0;  // Split: rows per (pass 1, pass 2) pair
+    bool vec = true;         // 16-byte units (true) or element units
+    int u = 1;               // elements per unit
+    bool forced = false;
+};
+
+// Launch one kernel of the given kind for a dtype combination.  `grid` is the
+// number of CTAs; Cluster launches use a.cs as the cluster size.
+template <Dt DI, Dt DO>
+cudaError_t launch_softmax(Kind k, const RowArgs &a, int g, bool vec, int64_t grid,
+                           cudaStream_t st);
+template <Dt D, bool FUSED>
+cudaError_t launch_rmsnorm(Kind k, const RowArgs &a, int g, bool vec, int64_t grid,
+                           cudaStream_t st);
+
+// Resident clusters of cs CTAs the cluster kernel could have at once
+// (cudaOccupancyMaxActiveClusters); 0 means the shape cannot be scheduled.
+template <Dt DI, Dt DO>
+cudaError_t softmax_cluster_occupancy(int g, bool vec, int cs, int *n);
+template <Dt D, bool FUSED>
+cudaError_t rmsnorm_cluster_occupancy(int g, bool vec, int cs, int *n);
+
+}  // namespace osr

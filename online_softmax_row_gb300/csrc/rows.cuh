@@ -1,0 +1,235 @@
+// rows.cuh -- register-cached row kernels: each row (or, in the cluster
+// tier, each piece of a row) is read from HBM exactly once into registers,
+// reduced, rescaled in registers and written exactly once.
+//
+// Geometry (template parameter G = threads per row or per row piece):
+//   G <= 32  : a group of G lanes per row, 128-thread CTAs holding 128/G rows
+//              ("several rows per warp" for short rows, "one warp per row");
+//   G >= 64  : one CTA of G threads per row, warp butterflies + one
+//              shared-memory stage ("one block per row");
+//   CLUSTER  : a thread-block cluster of cs CTAs per row, CTA partials
+//              merged through distributed shared memory, so a row longer
+//              than one CTA's registers is still read once ("several blocks
+//              per row", split-row).
+// Row-length policy of "Softmax 与归一化" (anrans.github.io), table
+// "按行长度选择并行方式"; register row cache of "两个融合算子：RMSNorm 与
+// online softmax" (daleiyang.github.io), §4·三 "N3：把 x 留在寄存器".
+//
+// Each thread owns EPT elements of its row as units of U elements (U = 16
+// bytes of input for the vector path, U = 1 for the element-wise path); unit
+// j of thread t is unit (u0 + j * G + t), so consecutive lanes touch
+// consecutive 16-byte vectors (coalesced).
+#pragma once
+
+#include "reduce.cuh"
+
+namespace osr {
+
+struct RowArgs {
+    const void *x;      // input rows
+    void *res;          // fused: residual, read and overwritten
+    const void *gamma;  // norms: [N] scale
+    void *y;            // output rows
+    float *row_max;     // softmax statistics, may be null
+    float *row_sum;
+    void *ws;           // split tier: per-piece partial states
+    int64_t M;          // rows
+    int64_t N;          // row length in elements
+    int64_t row0;       // first row handled by this launch (split batches)
+    int64_t chunk;      // cluster / split: units per CTA piece
+    int cs;             // cluster: CTAs per row; split: pieces per row
+    float eps;
+};
+
+template <int G>
+struct RowsGeom {
+    static constexpr int kThreads = G <= 32 ? 128 : G;
+    static constexpr int kRowsPerCta = kThreads / G;
+    static constexpr int kWarps = kThreads / 32;
+};
+
+struct Slice {
+    int64_t row;
+    int64_t u0, u1;  // unit range of this CTA's piece of the row
+    int t;           // thread index within the row group
+    bool ok;         // the row exists
+};
+
+template <int G, bool CLUSTER>
+__device__ __forceinline__ Slice make_slice(const RowArgs &a, int64_t nunits) {
+    Slice s;
+    if constexpr (G <= 32) {
+        s.row = (int64_t)blockIdx.x * RowsGeom<G>::kRowsPerCta + threadIdx.x / G;
+        s.t = threadIdx.x & (G - 1);
+        s.u0 = 0;
+        s.u1 = nunits;
+    } else if constexpr (!CLUSTER) {
+        s.row = blockIdx.x;
+        s.t = threadIdx.x;
+        s.u0 = 0;
+        s.u1 = nunits;
+    } else {
+        // 1-D grid, cluster dims (cs, 1, 1): CTAs [r*cs, (r+1)*cs) form the
+        // cluster of row r and %cluster_ctarank == blockIdx.x % cs
+        s.row = blockIdx.x / a.cs;
+        s.t = threadIdx.x;
+        s.u0 = (int64_t)cluster_ctarank() * a.chunk;
+        s.u1 = s.u0 + a.chunk < nunits ? s.u0 + a.chunk : nunits;
+    }
+    s.ok = s.row < a.M;
+    return s;
+}
+
+// ============================================================ softmax
+// Per thread: chunk summary of its cached elements (max, then sum of
+// exp(x - max), overwriting the cache with those exps) -- the chunk-summary
+// form of "两个融合算子" §4·四 "S4" with the chunk = the thread's elements.
+// The (m, d) states are merged across the row; then each thread rescales its
+// cached exps by exp(m_t - m) / d, so every element costs one exp.
+template <Dt DI, Dt DO, int G, int EPT, int U, bool CLUSTER>
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads)
+softmax_rows_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Slice s = make_slice<G, CLUSTER>(a, nunits);
+    const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+
+    float v[NU][U];
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (s.ok && ui < s.u1) {
+            load_unit<DI, U>(xrow, ui * U, v[j]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;  // contributes e^-inf = 0
+        }
+    }
+
+    float mt = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+#pragma unroll
+        for (int k = 0; k < U; ++k) mt = fmaxf(mt, v[j][k]);
+    float dt = 0.f;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            v[j][k] = expf(v[j][k] - mt);
+            dt += v[j][k];
+        }
+
+    MD st{mt, dt};
+    if constexpr (G <= 32) {
+        st = group_md<G>(st);
+    } else {
+        __shared__ float2 red[32];
+        st = block_md<RowsGeom<G>::kWarps>(st, red);
+    }
+    if constexpr (CLUSTER) {
+        __shared__ float2 slot;
+        st = cluster_md(st, a.cs, &slot);
+    }
+
+    const float scale = expf(mt - st.m) / st.d;
+    if (a.row_max != nullptr && s.ok && s.t == 0 && s.u0 == 0) {
+        a.row_max[s.row] = st.m;
+        if (a.row_sum != nullptr) a.row_sum[s.row] = st.d;
+    }
+
+    char *yrow = reinterpret_cast<char *>(a.y) + s.row * a.N * Elem<DO>::kBytes;
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (s.ok && ui < s.u1) {
+            float o[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) o[k] = v[j][k] * scale;
+            store_unit<DO, U>(yrow, ui * U, o);
+        }
+    }
+    if constexpr (CLUSTER) cluster_wait_acquire();
+}
+
+// ============================================================ RMSNorm
+// y = x * rsqrt(mean(x^2) + eps) * gamma; with FUSED, x + residual is first
+// rounded to the storage type, written back to the residual, and the
+// rounded sum is what gets normalised ("GPU Kernel 工程（04）" 八.3 "fused
+// residual + RMSNorm"; the stored value is normalised so that the output
+// equals RMSNorm of the new residual).
+template <Dt D, int G, int EPT, int U, bool CLUSTER, bool FUSED>
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads)
+rmsnorm_rows_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Slice s = make_slice<G, CLUSTER>(a, nunits);
+    const int64_t row_off = s.row * a.N * Elem<D>::kBytes;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+
+    float v[NU][U];
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (s.ok && ui < s.u1) {
+            load_unit<D, U>(xrow, ui * U, v[j]);
+            if constexpr (FUSED) {
+                char *rrow = reinterpret_cast<char *>(a.res) + row_off;
+                float r[U];
+                load_unit<D, U>(rrow, ui * U, r);
+#pragma unroll
+                for (int k = 0; k < U; ++k) v[j][k] = round_to<D>(v[j][k] + r[k]);
+                store_unit<D, U>(rrow, ui * U, v[j]);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) v[j][k] = 0.f;
+        }
+    }
+
+    // gamma is shared by every row: keep it cacheable (read-only path)
+    float g[NU][U];
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (s.ok && ui < s.u1) {
+            load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, g[j]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) g[j][k] = 0.f;
+        }
+    }
+
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+#pragma unroll
+        for (int k = 0; k < U; ++k) ss = fmaf(v[j][k], v[j][k], ss);
+
+    if constexpr (G <= 32) {
+        ss = group_sum<G>(ss);
+    } else {
+        __shared__ float red[32];
+        ss = block_sum<RowsGeom<G>::kWarps>(ss, red);
+    }
+    if constexpr (CLUSTER) {
+        __shared__ float2 slot;
+        ss = cluster_sum(ss, a.cs, &slot);
+    }
+    const float r = rsqrtf(ss / (float)a.N + a.eps);
+
+    char *yrow = reinterpret_cast<char *>(a.y) + row_off;
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (s.ok && ui < s.u1) {
+            float o[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) o[k] = v[j][k] * r * g[j][k];
+            store_unit<D, U>(yrow, ui * U, o);
+        }
+    }
+    if constexpr (CLUSTER) cluster_wait_acquire();
+}
+
+}  // namespace osr

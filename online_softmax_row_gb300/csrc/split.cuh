@@ -1,0 +1,205 @@
+// split.cuh -- split-row tier for rows of any length: a row is cut into S
+// pieces handled by S independent CTAs.
+//   pass 1: each CTA streams its piece and writes one partial state to the
+//           workspace ws[row][piece] -- (m, d) for softmax, the sum of
+//           squares for the norms (the fused norm also writes the new
+//           residual here);
+//   pass 2: each CTA merges the S partials of its row in a fixed order (so
+//           every piece of a row sees bit-identical statistics and repeated
+//           runs are bit-identical), then streams its piece again and writes
+//           the output.
+// "Softmax 与归一化" (anrans.github.io), table "按行长度选择并行方式" (the
+// "very long rows, few rows: several blocks per row, partial (m, d) then
+// merge" row) and "第23讲：为什么Attention必须先算Max？" (lilinji.mintlify.site)
+// §8.3 thought question 1 (rows beyond 65536).  The host keeps the second read
+// in L2 by issuing the two passes over batches of rows whose pieces fit L2.
+#pragma once
+
+#include "rows.cuh"
+
+namespace osr {
+
+template <int G>
+struct SplitGeom {
+    static constexpr int kThreads = G;
+    static constexpr int kWarps = G / 32;
+};
+
+// CTA (row, piece) of a split launch; rows are a.row0 + blockIdx.x / S.
+struct Piece {
+    int64_t row;
+    int p;
+    int64_t u0, u1;
+};
+
+__device__ __forceinline__ Piece make_piece(const RowArgs &a, int64_t nunits) {
+    Piece q;
+    q.row = a.row0 + blockIdx.x / a.cs;
+    q.p = blockIdx.x % a.cs;
+    q.u0 = (int64_t)q.p * a.chunk;
+    q.u1 = q.u0 + a.chunk < nunits ? q.u0 + a.chunk : nunits;
+    return q;
+}
+
+// ------------------------------------------------------------ softmax pass 1
+// Each tile of the piece is summarised (max, then sum of exp(x - max)) and
+// merged into the thread's running (m, d), the chunk-summary update of
+// "两个融合算子：RMSNorm 与 online softmax" §4·四 "S4".
+template <Dt DI, int G, int EPT, int U>
+__global__ void __launch_bounds__(G) softmax_split_stats_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    const char *xrow = reinterpret_cast<const char *>(a.x) + q.row * a.N * Elem<DI>::kBytes;
+    MD st = md_identity();
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                load_unit<DI, U, Hint::Keep>(xrow, ui * U, v[j]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
+            }
+        }
+        float tm = -FLT_MAX;
+#pragma unroll
+        for (int j = 0; j < NU; ++j)
+#pragma unroll
+            for (int k = 0; k < U; ++k) tm = fmaxf(tm, v[j][k]);
+        float td = 0.f;
+#pragma unroll
+        for (int j = 0; j < NU; ++j)
+#pragma unroll
+            for (int k = 0; k < U; ++k) td += expf(v[j][k] - tm);
+        st = md_merge(st, MD{tm, td});
+    }
+    __shared__ float2 red[32];
+    st = block_md<SplitGeom<G>::kWarps>(st, red);
+    if (threadIdx.x == 0)
+        reinterpret_cast<float2 *>(a.ws)[q.row * a.cs + q.p] = make_float2(st.m, st.d);
+}
+
+// ------------------------------------------------------------ softmax pass 2
+template <Dt DI, Dt DO, int G, int EPT, int U>
+__global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    // merge the row's S partials: thread i holds partial i (S <= G)
+    MD st = md_identity();
+    if (threadIdx.x < a.cs) {
+        const float2 w = reinterpret_cast<const float2 *>(a.ws)[q.row * a.cs + threadIdx.x];
+        st = MD{w.x, w.y};
+    }
+    __shared__ float2 red[32];
+    st = block_md<SplitGeom<G>::kWarps>(st, red);
+    if (a.row_max != nullptr && q.p == 0 && threadIdx.x == 0) {
+        a.row_max[q.row] = st.m;
+        if (a.row_sum != nullptr) a.row_sum[q.row] = st.d;
+    }
+    const float inv_d = 1.0f / st.d;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + q.row * a.N * Elem<DI>::kBytes;
+    char *yrow = reinterpret_cast<char *>(a.y) + q.row * a.N * Elem<DO>::kBytes;
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) load_unit<DI, U>(xrow, ui * U, v[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                float o[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) o[k] = expf(v[j][k] - st.m) * inv_d;
+                store_unit<DO, U>(yrow, ui * U, o);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ RMSNorm pass 1
+template <Dt D, int G, int EPT, int U, bool FUSED>
+__global__ void __launch_bounds__(G) rmsnorm_split_stats_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    const int64_t row_off = q.row * a.N * Elem<D>::kBytes;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    float ss = 0.f;
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                if constexpr (FUSED) {
+                    char *rrow = reinterpret_cast<char *>(a.res) + row_off;
+                    float r[U];
+                    load_unit<D, U>(xrow, ui * U, v[j]);
+                    load_unit<D, U>(rrow, ui * U, r);
+#pragma unroll
+                    for (int k = 0; k < U; ++k) v[j][k] = round_to<D>(v[j][k] + r[k]);
+                    store_unit<D, U>(rrow, ui * U, v[j]);
+                } else {
+                    load_unit<D, U, Hint::Keep>(xrow, ui * U, v[j]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < U; ++k) v[j][k] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NU; ++j)
+#pragma unroll
+            for (int k = 0; k < U; ++k) ss = fmaf(v[j][k], v[j][k], ss);
+    }
+    __shared__ float red[32];
+    ss = block_sum<SplitGeom<G>::kWarps>(ss, red);
+    if (threadIdx.x == 0) reinterpret_cast<float *>(a.ws)[q.row * a.cs + q.p] = ss;
+}
+
+// ------------------------------------------------------------ RMSNorm pass 2
+// Reads x (or, fused, the new residual written by pass 1) again.
+template <Dt D, int G, int EPT, int U, bool FUSED>
+__global__ void __launch_bounds__(G) rmsnorm_split_apply_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    float ss = 0.f;
+    if (threadIdx.x < a.cs) ss = reinterpret_cast<const float *>(a.ws)[q.row * a.cs + threadIdx.x];
+    __shared__ float red[32];
+    ss = block_sum<SplitGeom<G>::kWarps>(ss, red);
+    const float r = rsqrtf(ss / (float)a.N + a.eps);
+    const int64_t row_off = q.row * a.N * Elem<D>::kBytes;
+    const char *src = reinterpret_cast<const char *>(FUSED ? a.res : a.x) + row_off;
+    char *yrow = reinterpret_cast<char *>(a.y) + row_off;
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U], g[NU][U];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                load_unit<D, U>(src, ui * U, v[j]);
+                load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, g[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                float o[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) o[k] = v[j][k] * r * g[j][k];
+                store_unit<D, U>(yrow, ui * U, o);
+            }
+        }
+    }
+}
+
+}  // namespace osr

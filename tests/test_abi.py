@@ -1,0 +1,152 @@
+"""C-ABI checks that need no GPU: the library builds/loads, exports every
+entry point the headers declare, validates arguments before touching a
+device, and the length-based dispatcher picks the documented tier."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import online_softmax_row_gb300 as osr
+from online_softmax_row_gb300 import build as osr_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    osr_build.build()
+    return osr.library()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(osr_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_headers_declare_the_three_operations():
+    names = declared_symbols()
+    for n in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for s in range(7):
+        assert lib.osr_status_string(s)
+    assert lib.osr_version() >= 100
+
+
+# ------------------------------------------------------------ validation
+# These calls return before any CUDA call: pointers are never dereferenced.
+
+F32, BF16 = 0, 1
+P = 0x10000  # fake, never dereferenced
+
+
+def test_m_zero_is_noop(lib):
+    assert lib.osr_softmax_rows(None, None, 0, 5, F32, F32, None) == 0
+    assert lib.osr_rmsnorm_fwd(None, None, ctypes.c_float(1e-6), None, 0, 5, F32, None) == 0
+    assert lib.osr_fused_add_rmsnorm(None, None, None, ctypes.c_float(1e-6), None, 0, 5, BF16, None) == 0
+
+
+def test_invalid_sizes_and_dtypes(lib):
+    assert lib.osr_softmax_rows(P, P * 4, 1, 0, F32, F32, None) == 1       # N == 0
+    assert lib.osr_softmax_rows(P, P * 4, -1, 4, F32, F32, None) == 1      # M < 0
+    assert lib.osr_softmax_rows(P, P * 4, 1, 4, 7, F32, None) == 1         # dtype
+    assert lib.osr_softmax_rows(None, P, 1, 4, F32, F32, None) == 1        # NULL x
+    assert lib.osr_rmsnorm_fwd(P, None, ctypes.c_float(0), P * 4, 1, 4, F32, None) == 1
+    assert lib.osr_fused_add_rmsnorm(P, None, P * 2, ctypes.c_float(0), P * 4, 1, 4, F32, None) == 1
+
+
+def test_alias_rules(lib):
+    # softmax: partial overlap forbidden; in place needs equal dtypes
+    assert lib.osr_softmax_rows(P, P + 4, 4, 16, F32, F32, None) == 3
+    assert lib.osr_softmax_rows(P, P, 4, 16, BF16, F32, None) == 3
+    # rmsnorm: y overlapping gamma
+    assert lib.osr_rmsnorm_fwd(P, P * 2 + 8, ctypes.c_float(0), P * 2, 4, 16, F32, None) == 3
+    # fused: residual overlapping x / out
+    assert lib.osr_fused_add_rmsnorm(P, P + 64, P * 8, ctypes.c_float(0), P * 16, 4, 16, F32, None) == 3
+    assert lib.osr_fused_add_rmsnorm(P, P * 4, P * 8, ctypes.c_float(0), P * 4, 4, 16, F32, None) == 3
+    # stats overlapping x
+    assert lib.osr_softmax_rows_stats(P, P * 4, P, None, 4, 16, F32, F32, None) == 3
+
+
+def test_host_pointers_rejected(lib):
+    # plain host memory is not device memory: rejected before any launch
+    buf = (ctypes.c_float * 64)()
+    out = (ctypes.c_float * 64)()
+    a, b = ctypes.addressof(buf), ctypes.addressof(out)
+    assert lib.osr_softmax_rows(a, b, 4, 16, F32, F32, None) in (1, 5)
+
+
+def test_bench_copy_validation(lib):
+    assert lib.osr_bench_copy(P, P * 4, 0, None) == 0
+    assert lib.osr_bench_copy(P, P * 4, 24, None) == 1       # not a multiple of 16
+    assert lib.osr_bench_copy(P + 4, P * 4, 32, None) == 1   # misaligned
+    assert lib.osr_bench_copy(P, P + 16, 64, None) == 3      # overlap
+
+
+# ------------------------------------------------------------ dispatcher
+
+@pytest.mark.parametrize("n,tier", [
+    (1, "rows g=1"), (32, "rows g=2"), (128, "rows g=8"), (1024, "rows g=64"),
+    (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "cluster cs=2"),
+    (152064, "cluster cs=10"), (262144, "cluster cs=16"), (1 << 20, "split"),
+])
+def test_dispatch_tiers_f32(lib, n, tier):
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, n, "f32").startswith(tier)
+
+
+def test_dispatch_capacity_counts_cached_fp32_elements():
+    # the register cache holds widened binary32 values, so a bf16 row needs
+    # the same number of threads as an f32 row of the same length
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32").startswith("rows g=1024")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 32768, "bf16", "f32").startswith("cluster cs=2")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("cluster cs=10")
+
+
+def test_dispatch_scalar_path_when_misaligned():
+    assert osr.plan_describe(osr.OP_SOFTMAX, 8, 1023, "f32").endswith("scalar")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 8, 1024, "f32", vec_ok=False).endswith("scalar")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 8, 1024, "f32").endswith("vec")
+
+
+def test_dispatch_norms():
+    assert osr.plan_describe(osr.OP_FUSED, 8192, 4096, "bf16") == "rows g=256 ept=16 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 3584, "f32") == "rows g=256 ept=16 vec"
+    with pytest.raises(osr.OsrError):
+        osr.plan_describe(osr.OP_RMSNORM, 64, 3584, "f32", "bf16")
+
+
+def test_split_shape_bounds():
+    d = osr.plan_describe(osr.OP_SOFTMAX, 3, 10_000_000, "f32")
+    s = int(re.search(r"s=(\d+)", d).group(1))
+    b = int(re.search(r"b=(\d+)", d).group(1))
+    assert 1 <= s <= 512 and 1 <= b <= 3
+
+
+def test_forced_kernel(monkeypatch):
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "split:s=7,b=3")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("split s=7 b=3")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "cluster:g=256,cs=2")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("cluster cs=2 g=256")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "rows:g=512")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("rows g=512")
+    # a forced shape that cannot hold the row is refused, not silently changed
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "rows:g=64")
+    with pytest.raises(osr.OsrError) as e:
+        osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
+    assert e.value.name == "OSR_ERR_UNSUPPORTED"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "cluster:g=256,cs=1")
+    with pytest.raises(osr.OsrError):
+        osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
