@@ -43,12 +43,7 @@ def build(force: bool = False) -> str:
     return LIB
 
 
-def _load():
-    global _lib
-    with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
+def _configure(lib):
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         D = ctypes.c_double
@@ -64,8 +59,46 @@ def _load():
         lib.orc_softmax_online.argtypes = [P, I, I64, I64, P, P, P]
         lib.orc_md_merge.argtypes = [D, D, D, D, P, P]
         lib.orc_softmax_chunked_stats.argtypes = [P, I, I64, I64, I64, P, P]
-        _lib = lib
         return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
+
+
+def compile_variant(src_text: str, out_path: str) -> str:
+    """Compile a modified copy of oracle.c (used by the pin-strength tests,
+    which plant mistakes in a copy and check that the pins catch them)."""
+    src = out_path[:-3] + ".c"
+    with open(src, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", out_path,
+                    "-lm"], check=True)
+    return out_path
+
+
+class use_library:
+    """Context manager: route every oracle call to the library at `path`."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        with _lock:
+            self.saved = _lib
+            _lib = _configure(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.saved
 
 
 def _dt(a: np.ndarray) -> int:
