@@ -144,6 +144,43 @@ int osr_last_cuda_error(void);
 osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                              int vec_ok, int sm_count, char *buf, size_t buf_len);
 
+/*
+ * Row softmax that allocates nothing.
+ *
+ * No page this library follows has a counterpart of this call; it exists for
+ * callers that cannot allocate device memory while they run: serving loops
+ * that freeze their memory footprint after start-up, programs on devices or
+ * drivers without stream-ordered memory pools
+ * (cudaDevAttrMemoryPoolsSupported == 0), and code running inside another
+ * allocator's callbacks, where calling an allocator again can deadlock.
+ * osr_softmax_rows may take a small workspace from cudaMallocAsync; this call
+ * never calls cudaMalloc*, cudaFree* or any allocating routine.
+ *
+ * It computes what osr_softmax_rows computes (same arguments, dtypes,
+ * in-place and alias rules, same results within rounding) with the two-pass
+ * split-row kernels, keeping each row's per-piece (m, d) partials in one
+ * fixed device array of OSR_NOALLOC_MAX_PARTIALS pairs (8 bytes each,
+ * 512 KiB) compiled into the library.  Every GPU that loads the library holds
+ * that array until the process exits.
+ *   - M may be at most OSR_NOALLOC_MAX_PARTIALS; larger M returns
+ *     OSR_ERR_UNSUPPORTED before any device work.  Rows are cut into fewer
+ *     pieces when needed so that M x pieces fits the array.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps whatever the last call
+ *     wrote.  Nothing in it needs to start at zero: every slot a call reads
+ *     is written earlier in the same call.  Calls whose work overlaps on the
+ *     GPU (different streams, or different host threads on one device
+ *     without ordering between them) race on the array and may return wrong
+ *     results; order them on one stream or with events.
+ *   - A CUDA failure returns OSR_ERR_CUDA; osr_last_cuda_error() does not
+ *     report the code for this call.
+ */
+#define OSR_NOALLOC_MAX_PARTIALS 65536
+osr_status osr_softmax_rows_noalloc(const void *x, void *y, int64_t M, int64_t N,
+                                    osr_dtype in_dt, osr_dtype out_dt, void *stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int osr_version(void);
 
