@@ -201,6 +201,34 @@ def launches_per_call(plan: str, M: int) -> int:
     return 1
 
 
+def time_graph(osr, w, steps, warmup, device, l2_bytes):
+    """Device time of `steps` calls captured once in a CUDA graph and replayed
+    (rotating input sets): the kernels' own time without host launch cost."""
+    sets = make_sets(w, n_sets_for(w, l2_bytes), device)
+    for i in range(max(warmup, 3)):
+        call(osr, w, sets[i % len(sets)])
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            for i in range(steps):
+                call(osr, w, sets[i % len(sets)])
+    g.replay()
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(device)
+    start.record(cur)
+    g.replay()
+    stop.record(cur)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(stop)
+    del g, sets
+    torch.cuda.empty_cache()
+    return ms
+
+
 def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, sustain_s=0.0):
     """Device time of `steps` back-to-back calls (rotating input sets)."""
     sets = make_sets(w, n_sets_for(w, l2_bytes), device)
@@ -377,7 +405,8 @@ def ours(args):
                              props.multi_processor_count)
 
     elapsed_ms, clocks = time_workload(osr, w, args.steps, args.warmup, device, l2,
-                                       sampler_index=device.index, sustain_s=1.5)
+                                       sampler_index=None if args.profile else device.index,
+                                       sustain_s=0.0 if args.profile else 1.5)
     max_ms, total_bytes = aggregate_over_ranks(elapsed_ms, w.min_bytes * args.steps, world)
     value = total_bytes / (max_ms * 1e-3) / 1e9
     per_launch_ms = elapsed_ms / args.steps / launches_per_call(plan, w.M)
@@ -399,25 +428,27 @@ def ours(args):
         "gpu_launches": args.steps * launches_per_call(plan, w.M),
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_suite:
+    if rank == 0 and not (args.no_suite or args.profile):
         result["peaks"] = {"nominal_gbs": NOMINAL_HBM_GBS, "driver_measured_gbs": peak,
                            "copy_kernel_same_run_gbs": round(copy_peak(osr, device), 1)}
         suite = []
         for name, wl in workloads.WORKLOADS.items():
-            steps = max(10, min(200, int(2e9 * 20 / max(wl.min_bytes, 1) / 20)))
-            ms, _ = time_workload(osr, wl, steps, 5, device, l2)
+            steps = max(20, min(2000, int(1e10 / max(wl.min_bytes, 1))))
+            ms = time_graph(osr, wl, steps, 5, device, l2)
             p = osr.plan_describe(OP_CODE[wl.op], wl.M, wl.N, wl.in_dtype, wl.out_dtype, True,
                                   props.multi_processor_count)
             g = wl.min_bytes * steps / (ms * 1e-3) / 1e9
-            suite.append({"workload": name, "kernel": p, "min_bytes": wl.min_bytes,
+            suite.append({"workload": name, "kernel": p, "min_bytes": wl.min_bytes, "steps": steps,
+                          "timing": "CUDA graph of the steps, CUDA events around one replay",
                           "us_per_call": round(ms / steps * 1e3, 3), "gbs": round(g, 1),
                           "frac_measured": round(g / peak, 4), "frac_nominal": round(g / NOMINAL_HBM_GBS, 4),
                           "frac_copy_same_run": round(g / result["peaks"]["copy_kernel_same_run_gbs"], 4),
                           "launches_per_call": launches_per_call(p, wl.M)})
         result["per_kernel"] = suite
     if rank == 0:
-        result["e2e"] = time_e2e(osr, w, max(3, min(args.steps, 50)), args.warmup, device)
-        result["cpu_baseline"] = cpu_baseline_for(w)
+        if not args.profile:
+            result["e2e"] = time_e2e(osr, w, max(3, min(args.steps, 50)), args.warmup, device)
+            result["cpu_baseline"] = cpu_baseline_for(w)
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -469,6 +500,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-suite", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the timed steps of the workload (for ncu captures): no clock "
+                         "sampling, per-workload table, e2e or CPU baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -45,6 +45,39 @@ __device__ __forceinline__ float round_to(float v) {
     return v;
 }
 
+// ---------------------------------------------------------------- exp
+// e^(x - m) for x <= m, as 2^((x - m) log2 e) on the special-function unit
+// (PTX ex2.approx.ftz.f32: about 2 ulp; -inf -> 0; results below the normal
+// range flush to 0).  The difference is formed before scaling, so the only
+// extra error is the rounding of the product, |x - m| log2 e 2^-24 in the
+// exponent: 5e-6 relative at x - m = -80.
+__device__ __forceinline__ float ex2_approx(float t) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+__device__ __forceinline__ float exp_shifted(float x, float m) {
+    return ex2_approx((x - m) * 1.4426950408889634f);
+}
+
+// ---------------------------------------------------------------- packed bf16
+// Eight bfloat16 values in a 16-byte vector, element k in half (k & 1) of
+// word k / 2.  Widening is exact; packing rounds to nearest even.
+__device__ __forceinline__ void unpack8(const uint4 &q, float (&f)[8]) {
+    f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
+    f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
+    f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z);
+    f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 q;
+    q.x = pack_bf16x2(f[0], f[1]);
+    q.y = pack_bf16x2(f[2], f[3]);
+    q.z = pack_bf16x2(f[4], f[5]);
+    q.w = pack_bf16x2(f[6], f[7]);
+    return q;
+}
+
 // ---------------------------------------------------------------- loads
 // A "unit" is U consecutive elements: one 16-byte vector (U = kVec) or one
 // scalar (U = 1).  `e` is the element offset of the unit from `base`.

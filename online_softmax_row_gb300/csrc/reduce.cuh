@@ -13,12 +13,12 @@
 // identity, the -FLT_MAX substitute) and §3·三 "联合归约：把 (m, s) 当成一个整体";
 // "RMSNorm、Softmax 与在线归约" (notes.kuangjux.top), "从逐元素更新到合并两个 tile".
 //
-// Every exchange is an xor butterfly.  Because each merge below is exactly
-// commutative in floating point (a + b == b + a; the (m, d) merge picks the
-// larger m and scales the other side), the two partners of every butterfly
-// step compute the same value, so after the last step all lanes agree bit
-// for bit.  Block and cluster stages have every warp redo the final
-// butterfly on the same inputs, so all warps (and all CTAs) agree too.
+// Every exchange is an xor butterfly of an exactly commutative operation
+// (a + b == b + a, max), so the two partners of every butterfly step compute
+// the same value and after the last step all lanes agree bit for bit.  Block
+// and cluster stages have every warp redo the final butterfly on the same
+// inputs, so all warps (and all CTAs) agree too.  The pairwise merge itself
+// (md_merge) is used where one thread folds its own tiles in order.
 #pragma once
 
 #include "device_common.cuh"
@@ -52,20 +52,84 @@ __device__ __forceinline__ float group_sum(float v) {
 }
 
 template <int W>
-__device__ __forceinline__ MD group_md(MD s) {
+__device__ __forceinline__ float group_max(float v) {
 #pragma unroll
-    for (int off = W / 2; off > 0; off >>= 1) {
-        MD o;
-        o.m = __shfl_xor_sync(0xffffffffu, s.m, off);
-        o.d = __shfl_xor_sync(0xffffffffu, s.d, off);
-        s = md_merge(s, o);
+    for (int off = W / 2; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// ---------------------------------------------------------------- (m, d) by max, then sum
+// Reducing many (m_t, d_t) states with the merge is the same as taking
+// m = max_t m_t and then d = sum_t d_t e^(m_t - m): in the coordinates
+// T = d e^m of "两个融合算子" §5·三 the merge is (max, +), so the reduction
+// splits into a max-reduction and a sum-reduction of the rescaled d_t.  This
+// costs one exp per thread instead of one per butterfly step, and f = e^(m_t
+// - m) is exactly the factor the thread later scales its cached exps by.
+struct RowNorm {
+    float m;  // row maximum
+    float d;  // sum over the row of e^(x - m)
+    float f;  // e^(m_t - m) for this thread's own m_t
+};
+
+template <int W>
+__device__ __forceinline__ RowNorm group_norm(float mt, float dt) {
+    RowNorm r;
+    r.m = group_max<W>(mt);
+    r.f = expf(mt - r.m);
+    r.d = group_sum<W>(dt * r.f);
+    return r;
+}
+
+// NW warps per row: one shared-memory stage for the max, one for the sum.
+template <int NW>
+__device__ __forceinline__ RowNorm block_norm(float mt, float dt, float *red_m, float *red_d) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    RowNorm r;
+    float m = group_max<32>(mt);
+    if constexpr (NW > 1) {
+        if (lane == 0) red_m[warp] = m;
+        __syncthreads();
+        m = group_max<NW>(red_m[lane & (NW - 1)]);
     }
-    return s;
+    r.m = m;
+    r.f = expf(mt - m);
+    float d = group_sum<32>(dt * r.f);
+    if constexpr (NW > 1) {
+        if (lane == 0) red_d[warp] = d;
+        __syncthreads();
+        d = group_sum<NW>(red_d[lane & (NW - 1)]);
+    }
+    r.d = d;
+    return r;
+}
+
+// cs <= 16 CTAs per row: each publishes its CTA-level (m_c, d_c); after the
+// cluster barrier every warp reads them through distributed shared memory
+// (lane r and lane r + 16 read CTA r) and reduces max-then-sum.  The thread's
+// factor is recomputed against the row maximum.  Ends with the relaxed
+// arrive; the caller executes cluster_wait_acquire() before exiting.
+__device__ __forceinline__ RowNorm cluster_norm(float mt, RowNorm c, int cs, float2 *slot) {
+    if (threadIdx.x == 0) *slot = make_float2(c.m, c.d);
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    const int r = threadIdx.x & 15;
+    float pm = -FLT_MAX, pd = 0.f;
+    if (r < cs) {
+        const float2 q = ld_dsmem_f2(mapa_shared(smem_u32(slot), r));
+        pm = q.x;
+        pd = q.y;
+    }
+    RowNorm out;
+    out.m = group_max<16>(pm);
+    out.d = group_sum<16>(pd * expf(pm - out.m));
+    out.f = expf(mt - out.m);
+    cluster_arrive_relaxed();
+    return out;
 }
 
 // ---------------------------------------------------------------- in a CTA
-// NW warps share one row.  Stage 1: butterfly inside each warp.  Stage 2:
-// each warp's lane 0 parks its result in shared memory; after one barrier
+// NW warps share one row's sum.  Stage 1: butterfly inside each warp.  Stage
+// 2: each warp's lane 0 parks its result in shared memory; after one barrier
 // every warp reads all NW results and runs the same butterfly over them.
 // `red` is a 32-entry shared array used once per kernel.
 
@@ -79,40 +143,14 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return group_sum<NW>(red[lane & (NW - 1)]);
 }
 
-template <int NW>
-__device__ __forceinline__ MD block_md(MD s, float2 *red) {
-    s = group_md<32>(s);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if constexpr (NW == 1) return s;
-    if (lane == 0) red[warp] = make_float2(s.m, s.d);
-    __syncthreads();
-    const float2 r = red[lane & (NW - 1)];
-    return group_md<NW>(MD{r.x, r.y});
-}
-
 // ---------------------------------------------------------------- in a cluster
-// cs CTAs (cs <= 32) share one row.  Each CTA publishes its CTA-level result
-// in its own shared memory, the cluster barrier makes it visible, and every
-// warp of every CTA gathers the cs results through distributed shared memory
-// (lane r reads CTA r) and runs the same 32-lane butterfly on them.  The
-// relaxed arrive that follows marks "done reading peers"; the caller must
-// execute cluster_wait_acquire() once before it exits so that no CTA leaves
-// while a peer may still read its shared memory.
-
-__device__ __forceinline__ MD cluster_md(MD s, int cs, float2 *slot) {
-    if (threadIdx.x == 0) *slot = make_float2(s.m, s.d);
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    const int lane = threadIdx.x & 31;
-    MD q = md_identity();
-    if (lane < cs) {
-        const float2 r = ld_dsmem_f2(mapa_shared(smem_u32(slot), lane));
-        q = MD{r.x, r.y};
-    }
-    q = group_md<32>(q);
-    cluster_arrive_relaxed();
-    return q;
-}
+// cs CTAs (cs <= 32) share one row's sum of squares.  Each CTA publishes its
+// CTA-level sum in its own shared memory, the cluster barrier makes it
+// visible, and every warp of every CTA gathers the cs sums through
+// distributed shared memory (lane r reads CTA r) and runs the same 32-lane
+// butterfly on them.  The relaxed arrive that follows marks "done reading
+// peers"; the caller must execute cluster_wait_acquire() once before it
+// exits so that no CTA leaves while a peer may still read its shared memory.
 
 __device__ __forceinline__ float cluster_sum(float s, int cs, float2 *slot) {
     if (threadIdx.x == 0) *slot = make_float2(s, 0.f);

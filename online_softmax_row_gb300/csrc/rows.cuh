@@ -84,8 +84,9 @@ __device__ __forceinline__ Slice make_slice(const RowArgs &a, int64_t nunits) {
 // Per thread: chunk summary of its cached elements (max, then sum of
 // exp(x - max), overwriting the cache with those exps) -- the chunk-summary
 // form of "两个融合算子" §4·四 "S4" with the chunk = the thread's elements.
-// The (m, d) states are merged across the row; then each thread rescales its
-// cached exps by exp(m_t - m) / d, so every element costs one exp.
+// The row's (m, d) follows by max-then-sum over the row's threads (and CTAs);
+// each thread then rescales its cached exps by e^(m_t - m) / d, so every
+// element costs one exp.
 template <Dt DI, Dt DO, int G, int EPT, int U, bool CLUSTER>
 __global__ void __launch_bounds__(RowsGeom<G>::kThreads)
 softmax_rows_kernel(const RowArgs a) {
@@ -116,26 +117,26 @@ softmax_rows_kernel(const RowArgs a) {
     for (int j = 0; j < NU; ++j)
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            v[j][k] = expf(v[j][k] - mt);
+            v[j][k] = exp_shifted(v[j][k], mt);
             dt += v[j][k];
         }
 
-    MD st{mt, dt};
+    RowNorm rn;
     if constexpr (G <= 32) {
-        st = group_md<G>(st);
+        rn = group_norm<G>(mt, dt);
     } else {
-        __shared__ float2 red[32];
-        st = block_md<RowsGeom<G>::kWarps>(st, red);
+        __shared__ float red_m[32], red_d[32];
+        rn = block_norm<RowsGeom<G>::kWarps>(mt, dt, red_m, red_d);
     }
     if constexpr (CLUSTER) {
         __shared__ float2 slot;
-        st = cluster_md(st, a.cs, &slot);
+        rn = cluster_norm(mt, rn, a.cs, &slot);
     }
 
-    const float scale = expf(mt - st.m) / st.d;
+    const float scale = rn.f / rn.d;
     if (a.row_max != nullptr && s.ok && s.t == 0 && s.u0 == 0) {
-        a.row_max[s.row] = st.m;
-        if (a.row_sum != nullptr) a.row_sum[s.row] = st.d;
+        a.row_max[s.row] = rn.m;
+        if (a.row_sum != nullptr) a.row_sum[s.row] = rn.d;
     }
 
     char *yrow = reinterpret_cast<char *>(a.y) + s.row * a.N * Elem<DO>::kBytes;
@@ -158,53 +159,93 @@ softmax_rows_kernel(const RowArgs a) {
 // rounded sum is what gets normalised ("GPU Kernel 工程（04）" 八.3 "fused
 // residual + RMSNorm"; the stored value is normalised so that the output
 // equals RMSNorm of the new residual).
+// bfloat16 rows on the 16-byte path stay packed in registers (4 registers
+// per 8 elements) and are widened when used, which halves the cache's
+// register footprint and raises occupancy.
 template <Dt D, int G, int EPT, int U, bool CLUSTER, bool FUSED>
 __global__ void __launch_bounds__(RowsGeom<G>::kThreads)
 rmsnorm_rows_kernel(const RowArgs a) {
+    constexpr bool kPacked = D == Dt::BF16 && U == 8;
     constexpr int NU = EPT / U;
+    constexpr int NP = kPacked ? NU : 1;  // packed vectors held
+    constexpr int NF = kPacked ? 1 : NU;  // fp32 units held
     const int64_t nunits = a.N / U;
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const int64_t row_off = s.row * a.N * Elem<D>::kBytes;
     const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
 
-    float v[NU][U];
+    uint4 pk[NP], gp[NP];
+    float v[NF][U], g[NF][U];
 #pragma unroll
     for (int j = 0; j < NU; ++j) {
         const int64_t ui = s.u0 + (int64_t)j * G + s.t;
-        if (s.ok && ui < s.u1) {
-            load_unit<D, U>(xrow, ui * U, v[j]);
-            if constexpr (FUSED) {
-                char *rrow = reinterpret_cast<char *>(a.res) + row_off;
-                float r[U];
-                load_unit<D, U>(rrow, ui * U, r);
+        const bool in = s.ok && ui < s.u1;
+        if constexpr (kPacked) {
+            pk[j] = make_uint4(0, 0, 0, 0);
+            if (in) {
+                pk[j] = ld16<Hint::Stream>(xrow + ui * 16);
+                if constexpr (FUSED) {
+                    char *rrow = reinterpret_cast<char *>(a.res) + row_off;
+                    const uint4 rq = ld16<Hint::Stream>(rrow + ui * 16);
+                    float xf[8], rf[8];
+                    unpack8(pk[j], xf);
+                    unpack8(rq, rf);
 #pragma unroll
-                for (int k = 0; k < U; ++k) v[j][k] = round_to<D>(v[j][k] + r[k]);
-                store_unit<D, U>(rrow, ui * U, v[j]);
+                    for (int k = 0; k < 8; ++k) xf[k] += rf[k];
+                    pk[j] = pack8(xf);
+                    __stcs(reinterpret_cast<uint4 *>(rrow + ui * 16), pk[j]);
+                }
             }
         } else {
+            if (in) {
+                load_unit<D, U>(xrow, ui * U, v[j]);
+                if constexpr (FUSED) {
+                    char *rrow = reinterpret_cast<char *>(a.res) + row_off;
+                    float r[U];
+                    load_unit<D, U>(rrow, ui * U, r);
 #pragma unroll
-            for (int k = 0; k < U; ++k) v[j][k] = 0.f;
+                    for (int k = 0; k < U; ++k) v[j][k] = round_to<D>(v[j][k] + r[k]);
+                    store_unit<D, U>(rrow, ui * U, v[j]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < U; ++k) v[j][k] = 0.f;
+            }
         }
     }
 
-    // gamma is shared by every row: keep it cacheable (read-only path)
-    float g[NU][U];
+    // gamma is shared by every row: read-only path, fetched before the
+    // reduction so its latency overlaps it
 #pragma unroll
     for (int j = 0; j < NU; ++j) {
         const int64_t ui = s.u0 + (int64_t)j * G + s.t;
-        if (s.ok && ui < s.u1) {
-            load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, g[j]);
+        const bool in = s.ok && ui < s.u1;
+        if constexpr (kPacked) {
+            gp[j] = in ? ld16<Hint::ReadOnly>(reinterpret_cast<const char *>(a.gamma) + ui * 16)
+                       : make_uint4(0, 0, 0, 0);
         } else {
+            if (in) {
+                load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, g[j]);
+            } else {
 #pragma unroll
-            for (int k = 0; k < U; ++k) g[j][k] = 0.f;
+                for (int k = 0; k < U; ++k) g[j][k] = 0.f;
+            }
         }
     }
 
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < NU; ++j)
+    for (int j = 0; j < NU; ++j) {
+        if constexpr (kPacked) {
+            float f[8];
+            unpack8(pk[j], f);
 #pragma unroll
-        for (int k = 0; k < U; ++k) ss = fmaf(v[j][k], v[j][k], ss);
+            for (int k = 0; k < 8; ++k) ss = fmaf(f[k], f[k], ss);
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) ss = fmaf(v[j][k], v[j][k], ss);
+        }
+    }
 
     if constexpr (G <= 32) {
         ss = group_sum<G>(ss);
@@ -223,10 +264,19 @@ rmsnorm_rows_kernel(const RowArgs a) {
     for (int j = 0; j < NU; ++j) {
         const int64_t ui = s.u0 + (int64_t)j * G + s.t;
         if (s.ok && ui < s.u1) {
-            float o[U];
+            if constexpr (kPacked) {
+                float f[8], gf[8];
+                unpack8(pk[j], f);
+                unpack8(gp[j], gf);
 #pragma unroll
-            for (int k = 0; k < U; ++k) o[k] = v[j][k] * r * g[j][k];
-            store_unit<D, U>(yrow, ui * U, o);
+                for (int k = 0; k < 8; ++k) f[k] = f[k] * r * gf[k];
+                __stcs(reinterpret_cast<uint4 *>(yrow + ui * 16), pack8(f));
+            } else {
+                float o[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) o[k] = v[j][k] * r * g[j][k];
+                store_unit<D, U>(yrow, ui * U, o);
+            }
         }
     }
     if constexpr (CLUSTER) cluster_wait_acquire();

@@ -73,13 +73,13 @@ __global__ void __launch_bounds__(G) softmax_split_stats_kernel(const RowArgs a)
 #pragma unroll
         for (int j = 0; j < NU; ++j)
 #pragma unroll
-            for (int k = 0; k < U; ++k) td += expf(v[j][k] - tm);
+            for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], tm);
         st = md_merge(st, MD{tm, td});
     }
-    __shared__ float2 red[32];
-    st = block_md<SplitGeom<G>::kWarps>(st, red);
+    __shared__ float red_m[32], red_d[32];
+    const RowNorm rn = block_norm<SplitGeom<G>::kWarps>(st.m, st.d, red_m, red_d);
     if (threadIdx.x == 0)
-        reinterpret_cast<float2 *>(a.ws)[q.row * a.cs + q.p] = make_float2(st.m, st.d);
+        reinterpret_cast<float2 *>(a.ws)[q.row * a.cs + q.p] = make_float2(rn.m, rn.d);
 }
 
 // ------------------------------------------------------------ softmax pass 2
@@ -88,14 +88,16 @@ __global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a)
     constexpr int NU = EPT / U;
     const int64_t nunits = a.N / U;
     const Piece q = make_piece(a, nunits);
-    // merge the row's S partials: thread i holds partial i (S <= G)
+    // merge the row's S partials: thread i holds partial i (S <= G), the
+    // rest the identity; max-then-sum in a fixed tree
     MD st = md_identity();
     if (threadIdx.x < a.cs) {
         const float2 w = reinterpret_cast<const float2 *>(a.ws)[q.row * a.cs + threadIdx.x];
         st = MD{w.x, w.y};
     }
-    __shared__ float2 red[32];
-    st = block_md<SplitGeom<G>::kWarps>(st, red);
+    __shared__ float red_m[32], red_d[32];
+    const RowNorm rn = block_norm<SplitGeom<G>::kWarps>(st.m, st.d, red_m, red_d);
+    st = MD{rn.m, rn.d};
     if (a.row_max != nullptr && q.p == 0 && threadIdx.x == 0) {
         a.row_max[q.row] = st.m;
         if (a.row_sum != nullptr) a.row_sum[q.row] = st.d;
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a)
             if (ui < q.u1) {
                 float o[U];
 #pragma unroll
-                for (int k = 0; k < U; ++k) o[k] = expf(v[j][k] - st.m) * inv_d;
+                for (int k = 0; k < U; ++k) o[k] = exp_shifted(v[j][k], st.m) * inv_d;
                 store_unit<DO, U>(yrow, ui * U, o);
             }
         }
