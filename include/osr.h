@@ -72,7 +72,7 @@ typedef enum osr_status {
     OSR_ERR_ALIAS = 3,          /* buffers overlap in a way the call forbids */
     OSR_ERR_UNSUPPORTED = 4,    /* valid arguments outside what is implemented */
     OSR_ERR_CUDA = 5,           /* a CUDA call or launch failed: osr_last_cuda_error() */
-    OSR_ERR_DEVICE_TIMEOUT = 6  /* reserved: no kernel of this library waits on a flag */
+    OSR_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait ran out (see osr_device_fault) */
 } osr_status;
 
 /*
@@ -123,6 +123,18 @@ osr_status osr_softmax_rows(const void *x, void *y, int64_t M, int64_t N,
 osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float *row_sum,
                                   int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                                   void *stream);
+
+/*
+ * Device-side fault report.  The staged softmax tier (rows longer than 16384
+ * elements) waits for its bulk copies into shared memory with a bounded wait
+ * (1 s); if a wait ever runs out, the kernel records the fault in a device
+ * word, skips its stores and exits normally, so the context stays usable.
+ * This call synchronises `stream`, copies that word to *fault (0 = none),
+ * clears it, and returns OSR_ERR_DEVICE_TIMEOUT if it was set, OSR_OK if not
+ * (OSR_ERR_INVALID for a NULL fault pointer, OSR_ERR_CUDA on a CUDA error).
+ * The word is per device and shared by all streams of the process.
+ */
+osr_status osr_device_fault(void *stream, int *fault);
 
 /* Static description of a status code (never NULL). */
 const char *osr_status_string(osr_status s);

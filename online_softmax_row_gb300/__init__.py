@@ -15,6 +15,7 @@ softmax_rows         osr_softmax_rows
 softmax_rows_stats   osr_softmax_rows_stats
 plan_describe        osr_plan_describe
 bench_copy           osr_bench_copy
+device_fault         osr_device_fault
 """
 from __future__ import annotations
 
@@ -27,7 +28,8 @@ import torch
 from . import build as _build
 
 __all__ = ["OsrError", "rmsnorm_fwd", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
-           "plan_describe", "bench_copy", "library", "library_path", "OP_RMSNORM", "OP_FUSED",
+           "plan_describe", "bench_copy", "device_fault", "library", "library_path", "OP_RMSNORM",
+           "OP_FUSED",
            "OP_SOFTMAX"]
 
 OP_RMSNORM, OP_FUSED, OP_SOFTMAX = 0, 1, 2
@@ -73,8 +75,10 @@ def library():
         lib.osr_plan_describe.argtypes = [I, I64, I64, I, I, I, I, ctypes.c_char_p, ctypes.c_size_t]
         lib.osr_version.restype = I
         lib.osr_bench_copy.argtypes = [P, P, ctypes.c_size_t, P]
+        lib.osr_device_fault.argtypes = [P, ctypes.POINTER(I)]
         for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
-                   "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy"):
+                   "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy",
+                   "osr_device_fault"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -89,8 +93,24 @@ def _check(status: int, where: str):
         raise OsrError(status, where, detail)
 
 
-def _stream(t: torch.Tensor) -> int:
-    return torch.cuda.current_stream(t.device).cuda_stream
+_raw_stream_fn = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _raw_stream(index: int) -> int:
+    """cudaStream_t of torch's current stream on device `index`."""
+    if _raw_stream_fn is not None:
+        return _raw_stream_fn(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
+def _run(t: torch.Tensor, fn, *args):
+    """Call a C entry point with the tensor's device current and its current
+    stream appended as the last argument."""
+    index = t.device.index
+    if index is None or index == torch.cuda.current_device():
+        return fn(*args, _raw_stream(torch.cuda.current_device() if index is None else index))
+    with torch.cuda.device(index):
+        return fn(*args, _raw_stream(index))
 
 
 def _rows(t: torch.Tensor, name: str):
@@ -119,9 +139,9 @@ def rmsnorm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
     elif out.shape != x.shape or out.dtype != x.dtype:
         raise OsrError(1, "out", "shape/dtype must match x")
     _rows(out, "out")
-    with torch.cuda.device(x.device):
-        _check(library().osr_rmsnorm_fwd(x.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
-                                         M, H, _DT[x.dtype], _stream(x)), "osr_rmsnorm_fwd")
+    lib = _lib or library()
+    _check(_run(x, lib.osr_rmsnorm_fwd, x.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
+                M, H, _DT[x.dtype]), "osr_rmsnorm_fwd")
     return out
 
 
@@ -140,10 +160,9 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tens
     elif out.shape != x.shape or out.dtype != x.dtype:
         raise OsrError(1, "out", "shape/dtype must match x")
     _rows(out, "out")
-    with torch.cuda.device(x.device):
-        _check(library().osr_fused_add_rmsnorm(x.data_ptr(), residual.data_ptr(), gamma.data_ptr(),
-                                               float(eps), out.data_ptr(), M, H, _DT[x.dtype],
-                                               _stream(x)), "osr_fused_add_rmsnorm")
+    lib = _lib or library()
+    _check(_run(x, lib.osr_fused_add_rmsnorm, x.data_ptr(), residual.data_ptr(), gamma.data_ptr(),
+                float(eps), out.data_ptr(), M, H, _DT[x.dtype]), "osr_fused_add_rmsnorm")
     return out
 
 
@@ -161,9 +180,9 @@ def softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None,
     """Softmax over the last dimension (float32 or bfloat16 in and out)."""
     M, N = _rows(x, "x")
     out = _softmax_out(x, out, out_dtype)
-    with torch.cuda.device(x.device):
-        _check(library().osr_softmax_rows(x.data_ptr(), out.data_ptr(), M, N, _DT[x.dtype],
-                                          _DT[out.dtype], _stream(x)), "osr_softmax_rows")
+    lib = _lib or library()
+    _check(_run(x, lib.osr_softmax_rows, x.data_ptr(), out.data_ptr(), M, N, _DT[x.dtype],
+                _DT[out.dtype]), "osr_softmax_rows")
     return out
 
 
@@ -175,10 +194,9 @@ def softmax_rows_stats(x: torch.Tensor, out: torch.Tensor | None = None,
     lead = x.shape[:-1]
     row_max = torch.empty(lead, dtype=torch.float32, device=x.device)
     row_sum = torch.empty(lead, dtype=torch.float32, device=x.device)
-    with torch.cuda.device(x.device):
-        _check(library().osr_softmax_rows_stats(x.data_ptr(), out.data_ptr(), row_max.data_ptr(),
-                                                row_sum.data_ptr(), M, N, _DT[x.dtype],
-                                                _DT[out.dtype], _stream(x)), "osr_softmax_rows_stats")
+    lib = _lib or library()
+    _check(_run(x, lib.osr_softmax_rows_stats, x.data_ptr(), out.data_ptr(), row_max.data_ptr(),
+                row_sum.data_ptr(), M, N, _DT[x.dtype], _DT[out.dtype]), "osr_softmax_rows_stats")
     return out, row_max, row_sum
 
 
@@ -196,6 +214,17 @@ def bench_copy(src: torch.Tensor, dst: torch.Tensor) -> None:
     nbytes = src.numel() * src.element_size()
     if dst.numel() * dst.element_size() != nbytes:
         raise OsrError(1, "bench_copy", "sizes differ")
-    with torch.cuda.device(src.device):
-        _check(library().osr_bench_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream(src)),
-               "osr_bench_copy")
+    _check(_run(src, library().osr_bench_copy, src.data_ptr(), dst.data_ptr(), nbytes),
+           "osr_bench_copy")
+
+
+def device_fault(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device's
+    fault word: 0 if no kernel's bounded wait has run out since the last call."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    v = ctypes.c_int(0)
+    with torch.cuda.device(dev):
+        st = library().osr_device_fault(torch.cuda.current_stream(dev).cuda_stream, ctypes.byref(v))
+    if st not in (0, 6):
+        _check(st, "osr_device_fault")
+    return v.value

@@ -96,6 +96,43 @@ bool parse_kv(const char *s, const char *key, int64_t *v) {
     return false;
 }
 
+int64_t pow2_at_least(int64_t v) {
+    int64_t c = 1;
+    while (c < v) c <<= 1;
+    return c;
+}
+
+// Staged tier shape: the fewest CTAs per row whose pieces fit 96 KiB (or,
+// failing that, 200 KiB), raised until the grid has about three CTAs per SM
+// and rounded up to a power of two, which packs the GPCs better (measured:
+// 152064-element rows ran 13 % faster as 8 pieces than as 7).  force_cs: 0
+// decide.  Returns false if no piece within the limits holds the row.
+bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, int64_t force_cs, Plan *p) {
+    const int64_t row_bytes = nunits * 16;
+    int64_t cs = force_cs;
+    if (cs <= 0) {
+        int64_t need = cdiv(row_bytes, kStagedPreferBytes);
+        if (need > max_cluster) need = cdiv(row_bytes, kStagedMaxSmem - 128);
+        int64_t fill = cdiv(3 * (int64_t)sms, M);
+        const int64_t most = cdiv(nunits, kStagedThreads);
+        if (fill > most) fill = most;
+        if (fill > max_cluster) fill = max_cluster;
+        cs = need > fill ? need : fill;
+        const int64_t c2 = pow2_at_least(cs);
+        if (c2 <= max_cluster && cdiv(nunits, c2) >= kStagedThreads / 4) cs = c2;
+    }
+    if (cs < 1 || cs > max_cluster) return false;
+    const int64_t chunk = cdiv(nunits, cs);
+    const int64_t smem = 128 + chunk * 16;
+    if (smem > kStagedMaxSmem) return false;
+    p->tier = Tier::Staged;
+    p->g = kStagedThreads;
+    p->cs = (int)cs;
+    p->chunk = chunk;
+    p->smem = (size_t)smem;
+    return true;
+}
+
 void split_shape(int64_t M, int64_t N, int64_t nunits, int upt, int in_bytes, int sms,
                  int64_t force_s, int64_t force_b, Plan *p) {
     const int64_t row_bytes = N * in_bytes;
@@ -120,7 +157,6 @@ void split_shape(int64_t M, int64_t N, int64_t nunits, int upt, int in_bytes, in
 
 osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt, bool vec,
                      int sms, int max_cluster, Plan *p) {
-    (void)op;
     (void)out_dt;
     *p = Plan();
     p->vec = vec;
@@ -152,6 +188,12 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
             if (p->chunk > g * upt) return OSR_ERR_UNSUPPORTED;
             return OSR_OK;
         }
+        if (strncmp(force, "staged", 6) == 0) {
+            if (op != Op::Softmax || !vec) return OSR_ERR_UNSUPPORTED;
+            parse_kv(force, "cs", &cs);
+            if (cs <= 0) cs = 0;
+            return staged_shape(M, nunits, sms, max_cluster, cs, p) ? OSR_OK : OSR_ERR_UNSUPPORTED;
+        }
         if (strncmp(force, "split", 5) == 0) {
             parse_kv(force, "s", &s);
             parse_kv(force, "b", &b);
@@ -169,7 +211,10 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
         p->g = g;
         return OSR_OK;
     }
-    // 2. a cluster of 1024-thread CTAs, still register-cached (one read)
+    // 2. softmax on 16-byte rows: a cluster per row, pieces staged in shared
+    //    memory by bulk copies (one read)
+    if (op == Op::Softmax && vec && staged_shape(M, nunits, sms, max_cluster, 0, p)) return OSR_OK;
+    // 3. a cluster of 1024-thread CTAs, still register-cached (one read)
     const int64_t cs = cdiv(nunits, (int64_t)1024 * upt);
     if (cs <= max_cluster) {
         p->tier = Tier::Cluster;
@@ -178,7 +223,7 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
         p->chunk = cdiv(nunits, cs);
         return OSR_OK;
     }
-    // 3. two passes through a workspace
+    // 4. two passes through a workspace
     split_shape(M, N, nunits, upt, in_bytes, sms, 0, 0, p);
     return OSR_OK;
 }
@@ -195,6 +240,9 @@ void describe(const Plan &p, char *buf, size_t n) {
     case Tier::Split:
         snprintf(buf, n, "split s=%d b=%lld g=%d ept=%d %s", p.cs, (long long)p.batch_rows, p.g,
                  kEpt, v);
+        break;
+    case Tier::Staged:
+        snprintf(buf, n, "staged cs=%d g=%d piece=%lldB %s", p.cs, p.g, (long long)p.chunk * 16, v);
         break;
     }
 }
@@ -241,15 +289,26 @@ cudaError_t cluster_occupancy(Op op, osr_dtype in_dt, osr_dtype out_dt, const Pl
 // A cluster plan whose cluster shape the device cannot schedule becomes a
 // split plan (or, if it was forced, an OSR_ERR_UNSUPPORTED).  Results of the
 // occupancy query are cached per device and kernel shape.
+cudaError_t staged_occupancy(osr_dtype in_dt, osr_dtype out_dt, const Plan &p, int *n) {
+    if (in_dt == OSR_F32 && out_dt == OSR_F32)
+        return softmax_staged_occupancy<Dt::F32, Dt::F32>(p.cs, p.smem, n);
+    if (in_dt == OSR_F32 && out_dt == OSR_BF16)
+        return softmax_staged_occupancy<Dt::F32, Dt::BF16>(p.cs, p.smem, n);
+    if (in_dt == OSR_BF16 && out_dt == OSR_F32)
+        return softmax_staged_occupancy<Dt::BF16, Dt::F32>(p.cs, p.smem, n);
+    return softmax_staged_occupancy<Dt::BF16, Dt::BF16>(p.cs, p.smem, n);
+}
+
 osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                               const DeviceInfo &di, Plan *p) {
-    if (p->tier != Tier::Cluster) return OSR_OK;
+    if (p->tier != Tier::Cluster && p->tier != Tier::Staged) return OSR_OK;
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, int, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, int, int, int, int, int, size_t>, int> cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    const auto key = std::make_tuple(dev, (int)op, (int)in_dt, (int)out_dt, p->g, (int)p->vec, p->cs);
+    const auto key = std::make_tuple(dev, (int)op, (int)in_dt, (int)out_dt, (int)p->tier, p->g,
+                                     (int)p->vec, p->cs, p->smem);
     int n = -1;
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -257,7 +316,8 @@ osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_
         if (it != cache.end()) n = it->second;
     }
     if (n < 0) {
-        e = cluster_occupancy(op, in_dt, out_dt, *p, &n);
+        e = p->tier == Tier::Staged ? staged_occupancy(in_dt, out_dt, *p, &n)
+                                    : cluster_occupancy(op, in_dt, out_dt, *p, &n);
         if (e != cudaSuccess) {
             cudaGetLastError();
             n = 0;
@@ -290,6 +350,23 @@ osr_status execute(Op op, osr_dtype in_dt, osr_dtype out_dt, RowArgs a, const Pl
         a.cs = p.cs;
         a.chunk = p.chunk;
         e = launch(op, in_dt, out_dt, Kind::Cluster, a, p, grid, st);
+        break;
+    }
+    case Tier::Staged: {
+        const int64_t grid = M * p.cs;
+        if (grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
+        a.cs = p.cs;
+        a.chunk = p.chunk;
+        const char *hook = getenv("OSR_TEST_HOOK");
+        if (hook && strcmp(hook, "no_arrive") == 0) a.flags |= kFlagNoArrive;
+        if (in_dt == OSR_F32 && out_dt == OSR_F32)
+            e = launch_softmax_staged<Dt::F32, Dt::F32>(a, grid, p.smem, st);
+        else if (in_dt == OSR_F32 && out_dt == OSR_BF16)
+            e = launch_softmax_staged<Dt::F32, Dt::BF16>(a, grid, p.smem, st);
+        else if (in_dt == OSR_BF16 && out_dt == OSR_F32)
+            e = launch_softmax_staged<Dt::BF16, Dt::F32>(a, grid, p.smem, st);
+        else
+            e = launch_softmax_staged<Dt::BF16, Dt::BF16>(a, grid, p.smem, st);
         break;
     }
     case Tier::Split: {

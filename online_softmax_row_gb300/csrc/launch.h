@@ -14,7 +14,9 @@ enum class Op : int { RmsNorm = 0, FusedAddRmsNorm = 1, Softmax = 2 };
 // Rows    : register-cached, one group / CTA per row        (one launch)
 // Cluster : register-cached, a CTA cluster per row (DSMEM)  (one launch)
 // Split   : S CTAs per row, partials in a workspace         (two launches)
-enum class Tier : int { Rows = 0, Cluster = 1, Split = 2 };
+// Staged  : softmax only, 16-byte rows: a cluster per row, each CTA's piece
+//           bulk-copied into shared memory                  (one launch)
+enum class Tier : int { Rows = 0, Cluster = 1, Split = 2, Staged = 3 };
 
 // Which kernel of a tier a launch runs.
 enum class Kind : int { Rows = 0, Cluster = 1, SplitStats = 2, SplitApply = 3 };
@@ -22,6 +24,9 @@ enum class Kind : int { Rows = 0, Cluster = 1, SplitStats = 2, SplitApply = 3 };
 constexpr int kEpt = 16;           // elements per thread per tile
 constexpr int kSplitThreads = 512;  // threads per split-row CTA
 constexpr int kMaxPieces = kSplitThreads;
+constexpr int kStagedThreads = 256;               // threads per staged CTA
+constexpr int kStagedPreferBytes = 96 << 10;      // piece size that leaves room for 2 CTAs/SM
+constexpr int kStagedMaxSmem = 200 << 10;         // largest staged piece + header
 
 struct Plan {
     Tier tier = Tier::Rows;
@@ -29,6 +34,7 @@ struct Plan {
     int cs = 1;              // Cluster: CTAs per row; Split: pieces per row
     int64_t chunk = 0;       // Cluster / Split: units per CTA piece
     int64_t batch_rows = 0;  // Split: rows per (pass 1, pass 2) pair
+    size_t smem = 0;         // Staged: dynamic shared memory per CTA
     bool vec = true;         // 16-byte units (true) or element units
     int u = 1;               // elements per unit
     bool forced = false;
@@ -49,5 +55,12 @@ template <Dt DI, Dt DO>
 cudaError_t softmax_cluster_occupancy(int g, bool vec, int cs, int *n);
 template <Dt D, bool FUSED>
 cudaError_t rmsnorm_cluster_occupancy(int g, bool vec, int cs, int *n);
+
+// Staged softmax tier (k_staged.cu): grid = rows * a.cs CTAs of
+// kStagedThreads, clusters of a.cs, `smem` bytes of dynamic shared memory.
+template <Dt DI, Dt DO>
+cudaError_t launch_softmax_staged(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st);
+template <Dt DI, Dt DO>
+cudaError_t softmax_staged_occupancy(int cs, size_t smem, int *n);
 
 }  // namespace osr

@@ -39,7 +39,12 @@ struct RowArgs {
     int64_t chunk;      // cluster / split: units per CTA piece
     int cs;             // cluster: CTAs per row; split: pieces per row
     float eps;
+    int flags;          // kFlag* test hooks (0 in normal use)
 };
+
+// Test hook: the staged tier's copy barrier gets no arrival, so its bounded
+// wait runs out and the kernel reports a fault instead of computing.
+constexpr int kFlagNoArrive = 1;
 
 template <int G>
 struct RowsGeom {

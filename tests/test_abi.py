@@ -100,19 +100,36 @@ def test_bench_copy_validation(lib):
 
 @pytest.mark.parametrize("n,tier", [
     (1, "rows g=1"), (32, "rows g=2"), (128, "rows g=8"), (1024, "rows g=64"),
-    (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "cluster cs=2"),
-    (152064, "cluster cs=10"), (262144, "cluster cs=16"), (1 << 20, "split"),
+    (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "staged cs=8"),
+    (152064, "staged cs=8"), (262144, "staged cs=16"), (1 << 20, "split"),
 ])
-def test_dispatch_tiers_f32(lib, n, tier):
+def test_dispatch_tiers_softmax_f32(lib, n, tier):
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, n, "f32").startswith(tier)
+
+
+@pytest.mark.parametrize("m,n,want", [
+    (2048, 32768, "staged cs=2 g=256 piece=65536B"),     # 2 pieces of 64 KiB
+    (441, 152064, "staged cs=8 g=256 piece=76032B"),     # fewest pieces <= 96 KiB, 2^k
+    (64, 152064, "staged cs=8 g=256 piece=76032B"),      # few rows: spread over 8 CTAs
+    (1, 32768, "staged cs=16 g=256 piece=8192B"),        # one row: spread over 16 CTAs
+    (3, 800000, "staged cs=16 g=256 piece=200000B"),     # largest pieces
+])
+def test_dispatch_staged_shapes(m, n, want):
+    assert osr.plan_describe(osr.OP_SOFTMAX, m, n, "f32").startswith(want)
+
+
+def test_dispatch_long_rows_without_staging():
+    # norms and misaligned rows keep the register-cached cluster tier
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "f32").startswith("cluster cs=2 g=1024")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 32768, "f32", vec_ok=False).startswith("cluster cs=2")
 
 
 def test_dispatch_capacity_counts_cached_fp32_elements():
     # the register cache holds widened binary32 values, so a bf16 row needs
     # the same number of threads as an f32 row of the same length
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32").startswith("rows g=1024")
-    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 32768, "bf16", "f32").startswith("cluster cs=2")
-    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("cluster cs=10")
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16").startswith("cluster cs=2")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("staged cs=8")
 
 
 def test_dispatch_scalar_path_when_misaligned():
@@ -148,5 +165,13 @@ def test_forced_kernel(monkeypatch):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
     assert e.value.name == "OSR_ERR_UNSUPPORTED"
     monkeypatch.setenv("OSR_FORCE_KERNEL", "cluster:g=256,cs=1")
+    with pytest.raises(osr.OsrError):
+        osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("staged cs=3 g=256 piece=6672B")
+    for bad in ((osr.OP_RMSNORM, True), (osr.OP_SOFTMAX, False)):  # softmax, 16-byte rows only
+        with pytest.raises(osr.OsrError):
+            osr.plan_describe(bad[0], 10, 5000, "f32", vec_ok=bad[1])
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=17")
     with pytest.raises(osr.OsrError):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")

@@ -141,7 +141,18 @@ def test_forced_tiers(spec, dt):
     check_fused(fi, out, res)
 
 
-@pytest.mark.parametrize("spec", ["cluster:g=1024,cs=16", "split:s=512,b=1"])
+@pytest.mark.parametrize("spec", ["staged:cs=1", "staged:cs=2", "staged:cs=5", "staged:cs=16",
+                                  "staged:cs=3", "staged:cs=8"])
+@pytest.mark.parametrize("io", [("f32", "f32"), ("bf16", "f32"), ("f32", "bf16"), ("bf16", "bf16")])
+def test_forced_staged(spec, io):
+    M, N = 37, 5000
+    inp = sm_case(M, N, io[0], seed_of("staged", spec, io))
+    y, rmax, rsum = run_forced(spec, lambda: osr.softmax_rows_stats(inp["x"].cuda(),
+                                                                    out_dtype=DT[io[1]]))
+    check_softmax(inp, y, rmax, rsum)
+
+
+@pytest.mark.parametrize("spec", ["cluster:g=1024,cs=16", "split:s=512,b=1", "staged:cs=16"])
 def test_forced_limits(spec):
     M, N = 3, 200000
     inp = sm_case(M, N, "f32", seed_of("limits", spec))
