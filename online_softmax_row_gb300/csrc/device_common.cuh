@@ -163,6 +163,18 @@ __device__ __forceinline__ void store_unit(void *base, int64_t e, const float (&
     }
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream drains;
+// griddepcontrol.wait blocks until that kernel has completed and its writes
+// are visible, so every kernel here calls it before its first global access
+// (without the launch attribute it returns at once).  launch_dependents,
+// issued after a CTA's last store, lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 // Thread-block cluster barrier (split arrive / wait) and distributed shared
 // memory access, as PTX.  Every thread of every CTA of the cluster executes

@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();
     const bool arrive = (a.flags & kFlagNoArrive) == 0;
     if (threadIdx.x == 0 && arrive) {
         // the input is read exactly once: fetch it under an evict-first L2
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
             store_unit<DO, U>(yrow, (u0 + u) * U, o);
         }
     }
+    pdl_trigger();
     cluster_wait_acquire();
 }
 
@@ -159,8 +161,10 @@ cudaLaunchConfig_t staged_config(int64_t grid, size_t smem, int cs, cudaStream_t
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
@@ -170,7 +174,7 @@ template <Dt DI, Dt DO>
 cudaError_t launch_softmax_staged(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st) {
     cudaError_t e = prepare<DI, DO>();
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = staged_config(grid, smem, a.cs, st, attr);
     return cudaLaunchKernelEx(&cfg, softmax_staged_kernel<DI, DO>, a);
 }
@@ -180,7 +184,7 @@ cudaError_t softmax_staged_occupancy(int cs, size_t smem, int *n) {
     *n = 0;
     cudaError_t e = prepare<DI, DO>();
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = staged_config((int64_t)cs * 64, smem, cs, nullptr, attr);
     return cudaOccupancyMaxActiveClusters(n, softmax_staged_kernel<DI, DO>, &cfg);
 }

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "rows.cuh"
 
@@ -27,6 +28,16 @@ constexpr int kMaxPieces = kSplitThreads;
 constexpr int kStagedThreads = 256;               // threads per staged CTA
 constexpr int kStagedPreferBytes = 96 << 10;      // piece size that leaves room for 2 CTAs/SM
 constexpr int kStagedMaxSmem = 200 << 10;         // largest staged piece + header
+
+// Launch with programmatic dependent launch (default on; OSR_PDL=0 turns it
+// off).  Read once per process.
+inline bool use_pdl() {
+    static const bool on = [] {
+        const char *e = getenv("OSR_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
 
 struct Plan {
     Tier tier = Tier::Rows;

@@ -99,6 +99,7 @@ softmax_rows_kernel(const RowArgs a) {
     const int64_t nunits = a.N / U;
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+    pdl_wait();
 
     float v[NU][U];
 #pragma unroll
@@ -155,6 +156,7 @@ softmax_rows_kernel(const RowArgs a) {
             store_unit<DO, U>(yrow, ui * U, o);
         }
     }
+    pdl_trigger();
     if constexpr (CLUSTER) cluster_wait_acquire();
 }
 
@@ -178,6 +180,7 @@ rmsnorm_rows_kernel(const RowArgs a) {
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const int64_t row_off = s.row * a.N * Elem<D>::kBytes;
     const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    pdl_wait();
 
     uint4 pk[NP], gp[NP];
     float v[NF][U], g[NF][U];
@@ -284,6 +287,7 @@ rmsnorm_rows_kernel(const RowArgs a) {
             }
         }
     }
+    pdl_trigger();
     if constexpr (CLUSTER) cluster_wait_acquire();
 }
 

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(G) softmax_split_stats_kernel(const RowArgs a)
     const int64_t nunits = a.N / U;
     const Piece q = make_piece(a, nunits);
     const char *xrow = reinterpret_cast<const char *>(a.x) + q.row * a.N * Elem<DI>::kBytes;
+    pdl_wait();
     MD st = md_identity();
     for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
         float v[NU][U];
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(G) softmax_split_stats_kernel(const RowArgs a)
     const RowNorm rn = block_norm<SplitGeom<G>::kWarps>(st.m, st.d, red_m, red_d);
     if (threadIdx.x == 0)
         reinterpret_cast<float2 *>(a.ws)[q.row * a.cs + q.p] = make_float2(rn.m, rn.d);
+    pdl_trigger();
 }
 
 // ------------------------------------------------------------ softmax pass 2
@@ -88,6 +90,7 @@ __global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a)
     constexpr int NU = EPT / U;
     const int64_t nunits = a.N / U;
     const Piece q = make_piece(a, nunits);
+    pdl_wait();
     // merge the row's S partials: thread i holds partial i (S <= G), the
     // rest the identity; max-then-sum in a fixed tree
     MD st = md_identity();
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a)
             }
         }
     }
+    pdl_trigger();
 }
 
 // ------------------------------------------------------------ RMSNorm pass 1
@@ -133,6 +137,7 @@ __global__ void __launch_bounds__(G) rmsnorm_split_stats_kernel(const RowArgs a)
     const Piece q = make_piece(a, nunits);
     const int64_t row_off = q.row * a.N * Elem<D>::kBytes;
     const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    pdl_wait();
     float ss = 0.f;
     for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
         float v[NU][U];
@@ -164,6 +169,7 @@ __global__ void __launch_bounds__(G) rmsnorm_split_stats_kernel(const RowArgs a)
     __shared__ float red[32];
     ss = block_sum<SplitGeom<G>::kWarps>(ss, red);
     if (threadIdx.x == 0) reinterpret_cast<float *>(a.ws)[q.row * a.cs + q.p] = ss;
+    pdl_trigger();
 }
 
 // ------------------------------------------------------------ RMSNorm pass 2
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__(G) rmsnorm_split_apply_kernel(const RowArgs a)
     constexpr int NU = EPT / U;
     const int64_t nunits = a.N / U;
     const Piece q = make_piece(a, nunits);
+    pdl_wait();
     float ss = 0.f;
     if (threadIdx.x < a.cs) ss = reinterpret_cast<const float *>(a.ws)[q.row * a.cs + threadIdx.x];
     __shared__ float red[32];
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(G) rmsnorm_split_apply_kernel(const RowArgs a)
             }
         }
     }
+    pdl_trigger();
 }
 
 }  // namespace osr
