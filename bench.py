@@ -443,7 +443,8 @@ def ours(args):
                           "us_per_call": round(ms / steps * 1e3, 3), "gbs": round(g, 1),
                           "frac_measured": round(g / peak, 4), "frac_nominal": round(g / NOMINAL_HBM_GBS, 4),
                           "frac_copy_same_run": round(g / result["peaks"]["copy_kernel_same_run_gbs"], 4),
-                          "launches_per_call": launches_per_call(p, wl.M)})
+                          "launches_per_call": launches_per_call(p, wl.M),
+                          "traffic": profiled_traffic(name)})
         result["per_kernel"] = suite
     if rank == 0:
         if not args.profile:
