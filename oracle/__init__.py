@@ -59,6 +59,8 @@ def _configure(lib):
         lib.orc_softmax_online.argtypes = [P, I, I64, I64, P, P, P]
         lib.orc_md_merge.argtypes = [D, D, D, D, P, P]
         lib.orc_softmax_chunked_stats.argtypes = [P, I, I64, I64, I64, P, P]
+        lib.orc_log_softmax.argtypes = [P, I, I64, I64, P]
+        lib.orc_logsumexp_argmax.argtypes = [P, I, I64, I64, P, P]
         return lib
 
 
@@ -212,3 +214,22 @@ def softmax_chunked_stats(x: np.ndarray, chunk: int):
     d = np.empty(M, dtype=np.float64)
     _load().orc_softmax_chunked_stats(_ptr(x), _dt(x), M, N, int(chunk), _ptr(m), _ptr(d))
     return m, d
+
+
+def log_softmax(x: np.ndarray):
+    """log softmax in binary64, as (x - m) - log d."""
+    x = _c(x)
+    M, N = _rows(x)
+    y = np.empty((M, N), dtype=np.float64)
+    _load().orc_log_softmax(_ptr(x), _dt(x), M, N, _ptr(y))
+    return y
+
+
+def logsumexp_argmax(x: np.ndarray):
+    """Per row: (m + log d) as float64 and the first index of the maximum."""
+    x = _c(x)
+    M, N = _rows(x)
+    lse = np.empty(M, dtype=np.float64)
+    am = np.empty(M, dtype=np.int64)
+    _load().orc_logsumexp_argmax(_ptr(x), _dt(x), M, N, _ptr(lse), _ptr(am))
+    return lse, am

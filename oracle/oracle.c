@@ -133,6 +133,27 @@ void orc_fused_add_rmsnorm(const void *x, const void *residual, const void *gamm
     }
 }
 
+/* Passes 1 and 2 of the three-pass safe softmax of [KJ] "稳定 Softmax" and
+ * [AZ] 七.2 for row i: m = max_j x_j (and the first j where it occurs),
+ * d = sum_j exp(x_j - m). */
+static void row_max_sum(const void *x, int dt, int64_t i, int64_t N, double *m_out,
+                        double *d_out, int64_t *at_out) {
+    double m = -INFINITY;
+    int64_t at = -1;
+    for (int64_t j = 0; j < N; ++j) {
+        double v = elem(x, dt, i * N + j);
+        if (v > m) {
+            m = v;
+            at = j;
+        }
+    }
+    double d = 0.0;
+    for (int64_t j = 0; j < N; ++j) d += exp(elem(x, dt, i * N + j) - m);
+    *m_out = m;
+    *d_out = d;
+    if (at_out) *at_out = at;
+}
+
 /* Safe softmax, three passes, [KJ] "稳定 Softmax" and [AZ] 七.2:
  *   m = max_j x_j,  d = sum_j exp(x_j - m),  y_i = exp(x_i - m) / d.
  * m_out/d_out (optional) receive m and d of each row. */
@@ -140,16 +161,41 @@ void orc_softmax(const void *x, int dt, int64_t M, int64_t N, double *y,
                  double *m_out, double *d_out) {
 #pragma omp parallel for schedule(static) num_threads(g_threads)
     for (int64_t i = 0; i < M; ++i) {
-        double m = -INFINITY;
-        for (int64_t j = 0; j < N; ++j) {
-            double v = elem(x, dt, i * N + j);
-            if (v > m) m = v;
-        }
-        double d = 0.0;
-        for (int64_t j = 0; j < N; ++j) d += exp(elem(x, dt, i * N + j) - m);
+        double m, d;
+        row_max_sum(x, dt, i, N, &m, &d, 0);
         for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + j) - m) / d;
         if (m_out) m_out[i] = m;
         if (d_out) d_out[i] = d;
+    }
+}
+
+/* Log-softmax: log y_i = (x_i - m) - log d with m and d of the three-pass
+ * definition (the logarithm of [KJ] "稳定 Softmax"; [AR] "Online softmax"
+ * notes that consumers such as samplers need only the statistics).  Written
+ * as (x_i - m) - log d so every intermediate is as small as the result. */
+void orc_log_softmax(const void *x, int dt, int64_t M, int64_t N, double *y) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double m, d;
+        row_max_sum(x, dt, i, N, &m, &d, 0);
+        const double ld = log(d);
+        for (int64_t j = 0; j < N; ++j) y[i * N + j] = (elem(x, dt, i * N + j) - m) - ld;
+    }
+}
+
+/* Row statistics a sampler needs without the probabilities: the
+ * log-sum-exp m + log d and the index of the row maximum (the first one on
+ * ties).  [AR] exercise 2 "大词表采样": greedy sampling needs only the
+ * argmax, so the full row of probabilities need not be written. */
+void orc_logsumexp_argmax(const void *x, int dt, int64_t M, int64_t N, double *lse,
+                          int64_t *argmax) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double m, d;
+        int64_t at;
+        row_max_sum(x, dt, i, N, &m, &d, &at);
+        if (lse) lse[i] = m + log(d);
+        if (argmax) argmax[i] = at;
     }
 }
 

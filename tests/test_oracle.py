@@ -396,3 +396,60 @@ def test_bit_helpers_agree_with_torch():
     t = torch.tensor([1.0, -2.5, 3.140625], dtype=torch.bfloat16)
     assert np.array_equal(bits_to_f64(bf16_bits(t)), t.double().numpy())
     assert list(itertools.islice(bf16_bits(t), 1)) == [0x3F80]
+
+
+# --------------------------------------------------------------- log-softmax, logsumexp, argmax
+
+def test_golden_logsumexp_1000_1001():
+    g = load_golden("logsumexp_1000_1001.txt")
+    tol = float(g["tol"])
+    x = f32(nums(g["x"]))
+    lse, am = oracle.logsumexp_argmax(x)
+    assert am[0] == int(g["expect.argmax"])
+    assert abs(lse[0] - (1001 + math.log(float(g["printed.d"])))) <= tol
+    ly = oracle.log_softmax(x)[0]
+    np.testing.assert_allclose(ly, [math.log(v) for v in nums(g["printed.y"])], rtol=0, atol=tol)
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 1000])
+def test_logsumexp_constant_row_closed_form(n):
+    # n equal entries c: lse = c + log n, every log-probability is -log n
+    c = 3.25
+    lse, am = oracle.logsumexp_argmax(np.full(n, c, np.float32))
+    assert abs(lse[0] - (c + math.log(n))) <= 1e-15 * (c + math.log(n))
+    assert am[0] == 0                                  # first index on ties
+    assert np.all(oracle.log_softmax(np.full(n, c, np.float32))[0] == -math.log(n))
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (3, 17), (8, 1000), (2, 4096)])
+def test_log_softmax_and_logsumexp_match_torch_fp64(shape):
+    g = torch.Generator().manual_seed(sum(shape) + 1)
+    x = torch.randn(*shape, generator=g) * 7
+    np.testing.assert_allclose(oracle.log_softmax(x.numpy()),
+                               torch.log_softmax(x.double(), -1).numpy(), rtol=1e-13, atol=1e-13)
+    lse, am = oracle.logsumexp_argmax(x.numpy())
+    np.testing.assert_allclose(lse, torch.logsumexp(x.double(), -1).numpy(), rtol=1e-15)
+    assert np.array_equal(am, np.argmax(x.numpy(), axis=1))
+
+
+def test_log_softmax_is_log_of_softmax_and_shift_invariant():
+    rng = np.random.default_rng(21)
+    x = (rng.integers(-8191, 8192, size=(4, 300)) / 1024.0).astype(np.float32)
+    ly = oracle.log_softmax(x)
+    np.testing.assert_allclose(np.exp(ly), oracle.softmax(x), rtol=1e-14)
+    xs = (x.astype(np.float64) + 1024.0).astype(np.float32)
+    assert np.array_equal(oracle.log_softmax(xs), ly)
+    lse, _ = oracle.logsumexp_argmax(x)
+    lse_s, _ = oracle.logsumexp_argmax(xs)
+    np.testing.assert_allclose(lse_s - 1024.0, lse, rtol=0, atol=1e-12)
+    _, m, d = oracle.softmax(x, return_stats=True)
+    np.testing.assert_allclose(lse, m + np.log(d), rtol=1e-15)
+
+
+def test_argmax_first_index_on_ties_and_minus_inf():
+    x = np.array([[1.0, 5.0, 5.0, 2.0], [-np.inf, -np.inf, 0.0, 0.0], [7.0, 7.0, 7.0, 7.0]],
+                 np.float32)
+    _, am = oracle.logsumexp_argmax(x)
+    assert list(am) == [1, 2, 0]
+    ly = oracle.log_softmax(x)
+    assert ly[1, 0] == -np.inf and abs(ly[1, 2] + math.log(2)) < 1e-15

@@ -24,11 +24,11 @@ MUTANTS = [
      "for (int64_t j = 0; j < N; ++j) d += exp(elem(x, dt, i * N + j) - m);",
      "for (int64_t j = 0; j < N; ++j) d += exp(elem(x, dt, i * N + j));"),
     ("min instead of max",
-     "            if (v > m) m = v;\n        }\n        double d = 0.0;",
-     "            if (v < m || m == -INFINITY) m = v;\n        }\n        double d = 0.0;"),
+     "        if (v > m) {\n            m = v;\n            at = j;",
+     "        if (v < m || m == -INFINITY) {\n            m = v;\n            at = j;"),
     ("output index reversed",
-     "for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + j) - m) / d;\n        if (m_out) m_out[i] = m;\n        if (d_out) d_out[i] = d;\n    }\n}\n\n/* Online",
-     "for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + (N - 1 - j)) - m) / d;\n        if (m_out) m_out[i] = m;\n        if (d_out) d_out[i] = d;\n    }\n}\n\n/* Online"),
+     "row_max_sum(x, dt, i, N, &m, &d, 0);\n        for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + j) - m) / d;",
+     "row_max_sum(x, dt, i, N, &m, &d, 0);\n        for (int64_t j = 0; j < N; ++j) y[i * N + j] = exp(elem(x, dt, i * N + (N - 1 - j)) - m) / d;"),
     ("online rescale with the wrong sign",
      "d = d * exp(m - mn) + exp(v - mn);",
      "d = d * exp(mn - m) + exp(v - mn);"),
@@ -50,6 +50,15 @@ MUTANTS = [
     ("fused normalises the unrounded sum",
      "h[j] = round_to(elem(x, dt, i * H + j) + elem(residual, dt, i * H + j), dt);",
      "h[j] = elem(x, dt, i * H + j) + elem(residual, dt, i * H + j);"),
+    ("log-softmax drops log d",
+     "y[i * N + j] = (elem(x, dt, i * N + j) - m) - ld;",
+     "y[i * N + j] = (elem(x, dt, i * N + j) - m);"),
+    ("logsumexp without the max",
+     "if (lse) lse[i] = m + log(d);",
+     "if (lse) lse[i] = log(d);"),
+    ("argmax takes the last index on ties",
+     "        if (v > m) {\n            m = v;\n            at = j;",
+     "        if (v >= m) {\n            m = v;\n            at = j;"),
     ("chunk summary sums exp without its max",
      "for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - cm);",
      "for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - m);"),
@@ -61,6 +70,8 @@ PARAMS = {
     "test_chunk_summaries_merge_to_row_statistics": [(7,), (64,)],
     "test_softmax_matches_torch_fp64": [((3, 17),), ((8, 1000),)],
     "test_rmsnorm_matches_torch_rms_norm_fp64": [((5, 33), "f32"), ((5, 33), "bf16")],
+    "test_logsumexp_constant_row_closed_form": [(7,)],
+    "test_log_softmax_and_logsumexp_match_torch_fp64": [((3, 17),)],
 }
 
 
