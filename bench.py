@@ -50,7 +50,7 @@ METRIC = "achieved HBM GB/s (min bytes) and % of GB300 HBM peak per kernel, 1 GP
 NOMINAL_HBM_GBS = 8000.0          # NVIDIA's public per-GPU HBM3e figure for GB300
 FALLBACK_HBM_GBS = 6800.0         # used only when no measured peak file exists
 DEFAULT_WORKLOAD = "fused_add_rmsnorm_bf16_8192x4096"
-OP_CODE = {"rmsnorm": 0, "fused_add_rmsnorm": 1, "softmax": 2}
+OP_CODE = {"rmsnorm": 0, "fused_add_rmsnorm": 1, "softmax": 2, "log_softmax": 3, "logsumexp": 4}
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -173,8 +173,11 @@ def make_sets(w, n_sets, device):
     for i in range(n_sets):
         inp = workloads.make(w, seed=i, device=device)
         s = dict(inp)
-        if w.op == "softmax":
+        if w.op in ("softmax", "log_softmax"):
             s["y"] = torch.empty(w.M, w.N, dtype=DT[w.out_dtype], device=device)
+        elif w.op == "logsumexp":
+            s["y"] = torch.empty(w.M, dtype=torch.float32, device=device)
+            s["arg"] = torch.empty(w.M, dtype=torch.int64, device=device)
         else:
             s["y"] = torch.empty_like(inp["x"])
         sets.append(s)
@@ -189,6 +192,17 @@ def n_sets_for(w, l2_bytes):
 def call(osr, w, s):
     if w.op == "softmax":
         return osr.softmax_rows(s["x"], out=s["y"])
+    if w.op == "log_softmax":
+        return osr.log_softmax_rows(s["x"], out=s["y"])
+    if w.op == "logsumexp":
+        lib = osr.library()
+        x = s["x"]
+        st = lib.osr_row_logsumexp(x.data_ptr(), s["y"].data_ptr(), s["arg"].data_ptr(), w.M, w.N,
+                                   1 if x.dtype == torch.bfloat16 else 0,
+                                   torch.cuda.current_stream(x.device).cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"osr_row_logsumexp: status {st}")
+        return s["y"]
     if w.op == "rmsnorm":
         return osr.rmsnorm_fwd(s["x"], s["gamma"], w.eps, out=s["y"])
     return osr.fused_add_rmsnorm(s["x"], s["residual"], s["gamma"], w.eps, out=s["y"])
@@ -281,7 +295,7 @@ def time_e2e(osr, w, steps, warmup, device):
     inp = workloads.make(w, seed=0, device="cpu")
     host_in = {k: v.pin_memory() for k, v in inp.items()}
     dev = {k: torch.empty_like(v, device=device) for k, v in inp.items()}
-    if w.op == "softmax":
+    if w.op in ("softmax", "log_softmax"):
         dev["y"] = torch.empty(w.M, w.N, dtype=DT[w.out_dtype], device=device)
     else:
         dev["y"] = torch.empty_like(dev["x"])
@@ -358,7 +372,7 @@ def cpu_baseline_for(w, budget_s=8.0):
 
 def _oracle_inputs(w, rows):
     """Oracle-format inputs (float32, or uint16 bf16 bits) for the first rows."""
-    if w.op == "softmax":
+    if w.op in ("softmax", "log_softmax", "logsumexp"):
         inp = workloads.softmax_inputs(rows, w.N, w.in_dtype, w.sigma, 0, w.shift, w.spikes_per_row,
                                        w.spike, seed=0)
     else:
@@ -374,6 +388,10 @@ def _run_oracle(oracle, w, inp):
     if w.op == "softmax":
         y = oracle.softmax(inp["x"])
         return oracle.round_to(y, w.out_dtype)
+    if w.op == "log_softmax":
+        return oracle.round_to(oracle.log_softmax(inp["x"]), w.out_dtype)
+    if w.op == "logsumexp":
+        return oracle.logsumexp_argmax(inp["x"])
     if w.op == "rmsnorm":
         y = oracle.rmsnorm(inp["x"], inp["gamma"], w.eps)
         return oracle.round_to(y, w.out_dtype)

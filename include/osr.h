@@ -136,6 +136,32 @@ osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float 
  */
 osr_status osr_device_fault(void *stream, int *fault);
 
+/*
+ * Row log-softmax: y[i, j] = (x[i, j] - m_i) - log d_i with m_i and d_i the
+ * row's normaliser statistics, computed by the same kernels (and dispatcher)
+ * as osr_softmax_rows.  Arguments, dtypes, in-place and alias rules as
+ * osr_softmax_rows.  -inf entries give -inf; a NaN entry makes its row NaN.
+ * The logarithm of the safe softmax of "RMSNorm、Softmax 与在线归约",
+ * "稳定 Softmax：归一化之前先减最大值", written so that every intermediate is as
+ * small as the result.
+ */
+osr_status osr_log_softmax_rows(const void *x, void *y, int64_t M, int64_t N, osr_dtype in_dt,
+                                osr_dtype out_dt, void *stream);
+
+/*
+ * Per-row sampling statistics without writing the probabilities:
+ *   lse    [M] binary32: log(sum_j exp(x[i, j])) = m_i + log d_i, may be NULL
+ *   argmax [M] int64:    the first j with x[i, j] = m_i, may be NULL
+ * (at least one of the two non-NULL).  Reads each row once; nothing else is
+ * written.  "Softmax 与归一化" (anrans.github.io), exercise 2 "大词表采样":
+ * greedy sampling needs only the argmax, so the softmax row need not be
+ * produced.  NaN entries are skipped by the maximum (and make lse NaN); a
+ * row of only -inf gives lse = -inf and argmax = -1.  x may have any dtype
+ * of osr_dtype; lse/argmax must not overlap x or each other.
+ */
+osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t M, int64_t N,
+                             osr_dtype in_dt, void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *osr_status_string(osr_status s);
 
@@ -145,7 +171,8 @@ int osr_last_cuda_error(void);
 
 /*
  * Which kernel the length-based dispatcher picks, without touching a GPU.
- *   op        0 = RMSNorm, 1 = fused residual-add + RMSNorm, 2 = softmax
+ *   op        0 = RMSNorm, 1 = fused residual-add + RMSNorm, 2 = softmax,
+ *             3 = log-softmax, 4 = log-sum-exp / argmax
  *   vec_ok    1 if every buffer is 16-byte aligned (the 128-bit path)
  *   sm_count  streaming multiprocessors of the target device (152 on GB300)
  *   buf       receives a NUL-terminated description, e.g.

@@ -13,6 +13,8 @@ rmsnorm_fwd          osr_rmsnorm_fwd
 fused_add_rmsnorm    osr_fused_add_rmsnorm
 softmax_rows         osr_softmax_rows
 softmax_rows_stats   osr_softmax_rows_stats
+log_softmax_rows     osr_log_softmax_rows
+row_logsumexp        osr_row_logsumexp
 plan_describe        osr_plan_describe
 bench_copy           osr_bench_copy
 device_fault         osr_device_fault
@@ -28,11 +30,12 @@ import torch
 from . import build as _build
 
 __all__ = ["OsrError", "rmsnorm_fwd", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
+           "log_softmax_rows", "row_logsumexp", "OP_LOG_SOFTMAX", "OP_LOGSUMEXP",
            "plan_describe", "bench_copy", "device_fault", "library", "library_path", "OP_RMSNORM",
            "OP_FUSED",
            "OP_SOFTMAX"]
 
-OP_RMSNORM, OP_FUSED, OP_SOFTMAX = 0, 1, 2
+OP_RMSNORM, OP_FUSED, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_LOGSUMEXP = 0, 1, 2, 3, 4
 _DT = {torch.float32: 0, torch.bfloat16: 1}
 _DT_NAME = {"f32": 0, "bf16": 1}
 _STATUS = {0: "OSR_OK", 1: "OSR_ERR_INVALID", 2: "OSR_ERR_ALIGN", 3: "OSR_ERR_ALIAS",
@@ -76,9 +79,11 @@ def library():
         lib.osr_version.restype = I
         lib.osr_bench_copy.argtypes = [P, P, ctypes.c_size_t, P]
         lib.osr_device_fault.argtypes = [P, ctypes.POINTER(I)]
+        lib.osr_log_softmax_rows.argtypes = [P, P, I64, I64, I, I, P]
+        lib.osr_row_logsumexp.argtypes = [P, P, P, I64, I64, I, P]
         for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
                    "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy",
-                   "osr_device_fault"):
+                   "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -198,6 +203,30 @@ def softmax_rows_stats(x: torch.Tensor, out: torch.Tensor | None = None,
     _check(_run(x, lib.osr_softmax_rows_stats, x.data_ptr(), out.data_ptr(), row_max.data_ptr(),
                 row_sum.data_ptr(), M, N, _DT[x.dtype], _DT[out.dtype]), "osr_softmax_rows_stats")
     return out, row_max, row_sum
+
+
+def log_softmax_rows(x: torch.Tensor, out: torch.Tensor | None = None,
+                     out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """Log-softmax over the last dimension: (x - max) - log(sum exp(x - max))."""
+    M, N = _rows(x, "x")
+    out = _softmax_out(x, out, out_dtype)
+    lib = _lib or library()
+    _check(_run(x, lib.osr_log_softmax_rows, x.data_ptr(), out.data_ptr(), M, N, _DT[x.dtype],
+                _DT[out.dtype]), "osr_log_softmax_rows")
+    return out
+
+
+def row_logsumexp(x: torch.Tensor, want_lse: bool = True, want_argmax: bool = True):
+    """Per row: log(sum exp(x)) (float32) and the first index of the maximum
+    (int64), reading x once and writing nothing else."""
+    M, N = _rows(x, "x")
+    lead = x.shape[:-1]
+    lse = torch.empty(lead, dtype=torch.float32, device=x.device) if want_lse else None
+    am = torch.empty(lead, dtype=torch.int64, device=x.device) if want_argmax else None
+    lib = _lib or library()
+    _check(_run(x, lib.osr_row_logsumexp, x.data_ptr(), lse.data_ptr() if lse is not None else None,
+                am.data_ptr() if am is not None else None, M, N, _DT[x.dtype]), "osr_row_logsumexp")
+    return lse, am
 
 
 def plan_describe(op: int, M: int, N: int, in_dtype: str = "f32", out_dtype: str | None = None,

@@ -228,6 +228,43 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
     return OSR_OK;
 }
 
+// Log-sum-exp / argmax geometry: the kernel streams, so any shape fits; it
+// only has to spread the rows.  Short rows: a group of g <= 32 lanes per row.
+// Otherwise one 256-thread CTA per row, and when there are fewer rows than
+// two per SM, a cluster of up to 8 CTAs per row (portable size).
+struct LsePlan {
+    int g = 1;
+    int cs = 1;
+    int64_t chunk = 0;
+    int64_t grid = 0;
+};
+
+LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
+    LsePlan lp;
+    const int u = vec ? vec_elems(in_dt) : 1;
+    const int64_t nunits = vec ? N / u : N;
+    const int upt = kEpt / u;
+    const int g = pow2ceil(cdiv(nunits, upt));
+    if (g <= 32) {
+        lp.g = g;
+        lp.grid = cdiv(M, 128 / g);
+        return lp;
+    }
+    lp.g = 256;
+    int64_t cs = 1;
+    if (M < 2 * (int64_t)sms) {
+        cs = pow2ceil(cdiv(2 * (int64_t)sms, M));
+        const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
+        if (cs > most) cs = most;
+        if (cs > 8) cs = 8;
+        if (cs < 1) cs = 1;
+    }
+    lp.cs = (int)cs;
+    lp.chunk = cdiv(nunits, cs);
+    lp.grid = M * cs;
+    return lp;
+}
+
 void describe(const Plan &p, char *buf, size_t n) {
     const char *v = p.vec ? "vec" : "scalar";
     switch (p.tier) {
@@ -450,15 +487,21 @@ int osr_version(void) { return 100; }
 
 osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                              int vec_ok, int sm_count, char *buf, size_t buf_len) {
-    if (op < 0 || op > 2 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
+    if (op < 0 || op > 4 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
         sm_count <= 0)
         return OSR_ERR_INVALID;
-    if (op != 2 && in_dt != out_dt) return OSR_ERR_UNSUPPORTED;
+    if (op < 2 && in_dt != out_dt) return OSR_ERR_UNSUPPORTED;
     osr_status s = check_sizes(M, N);
     if (s != OSR_OK) return s;
     const bool vec = vec_ok && (N % vec_elems(in_dt)) == 0;
+    if (op == 4) {
+        const LsePlan lp = lse_plan(M, N, in_dt, vec, sm_count);
+        snprintf(buf, buf_len, "%s g=%d cs=%d %s", lp.cs > 1 ? "lse-cluster" : "lse-rows", lp.g,
+                 lp.cs, vec ? "vec" : "scalar");
+        return OSR_OK;
+    }
     Plan p;
-    s = make_plan((Op)op, M, N, in_dt, out_dt, vec, sm_count, 16, &p);
+    s = make_plan(op >= 2 ? Op::Softmax : (Op)op, M, N, in_dt, out_dt, vec, sm_count, 16, &p);
     if (s != OSR_OK) return s;
     describe(p, buf, buf_len);
     return OSR_OK;
@@ -528,9 +571,9 @@ osr_status osr_fused_add_rmsnorm(const void *x, void *residual, const void *gamm
     return execute(Op::FusedAddRmsNorm, dt, dt, a, p, (cudaStream_t)stream);
 }
 
-osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float *row_sum,
-                                  int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
-                                  void *stream) {
+static osr_status softmax_entry(const void *x, void *y, float *row_max, float *row_sum,
+                                int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt, int flags,
+                                void *stream) {
     osr_status s = check_sizes(M, N);
     if (s != OSR_OK) return s;
     if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return OSR_ERR_INVALID;
@@ -561,7 +604,52 @@ osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float 
     a.row_sum = row_sum;
     a.M = M;
     a.N = N;
+    a.flags = flags;
     return execute(Op::Softmax, in_dt, out_dt, a, p, (cudaStream_t)stream);
+}
+
+osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float *row_sum,
+                                  int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
+                                  void *stream) {
+    return softmax_entry(x, y, row_max, row_sum, M, N, in_dt, out_dt, 0, stream);
+}
+
+osr_status osr_log_softmax_rows(const void *x, void *y, int64_t M, int64_t N, osr_dtype in_dt,
+                                osr_dtype out_dt, void *stream) {
+    return softmax_entry(x, y, nullptr, nullptr, M, N, in_dt, out_dt, kFlagLog, stream);
+}
+
+osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t M, int64_t N,
+                             osr_dtype in_dt, void *stream) {
+    osr_status s = check_sizes(M, N);
+    if (s != OSR_OK) return s;
+    if (!dtype_ok(in_dt)) return OSR_ERR_INVALID;
+    if (M == 0) return OSR_OK;
+    if (!x || (!lse && !argmax)) return OSR_ERR_INVALID;
+    const int64_t xb = M * N * elem_bytes(in_dt);
+    if ((lse && overlaps(lse, M * 4, x, xb)) || (argmax && overlaps(argmax, M * 8, x, xb)) ||
+        (lse && argmax && overlaps(lse, M * 4, argmax, M * 8)))
+        return OSR_ERR_ALIAS;
+    if (!device_accessible(x) || (lse && !device_accessible(lse)) ||
+        (argmax && !device_accessible(argmax)))
+        return OSR_ERR_INVALID;
+    DeviceInfo di;
+    if ((s = device_info(&di)) != OSR_OK) return s;
+    const bool vec = aligned16(x) && N % vec_elems(in_dt) == 0;
+    const LsePlan lp = lse_plan(M, N, in_dt, vec, di.sms);
+    if (lp.grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
+    RowArgs a = {};
+    a.x = x;
+    a.row_sum = lse;
+    a.row_arg = argmax;
+    a.M = M;
+    a.N = N;
+    a.cs = lp.cs;
+    a.chunk = lp.chunk;
+    const cudaError_t e = in_dt == OSR_F32
+        ? launch_lse<Dt::F32>(a, lp.g, lp.cs > 1, vec, lp.grid, (cudaStream_t)stream)
+        : launch_lse<Dt::BF16>(a, lp.g, lp.cs > 1, vec, lp.grid, (cudaStream_t)stream);
+    return e == cudaSuccess ? OSR_OK : cuda_fail(e);
 }
 
 osr_status osr_softmax_rows(const void *x, void *y, int64_t M, int64_t N, osr_dtype in_dt,

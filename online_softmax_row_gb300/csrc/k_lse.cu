@@ -1,0 +1,206 @@
+// k_lse.cu -- per-row log-sum-exp and argmax without writing probabilities.
+//
+// A sampler that draws greedily needs only the index of the row maximum, and
+// one that works in log space needs only log(sum_j e^(x_j)) = m + log d:
+// "Softmax 与归一化" (anrans.github.io), exercise 2 "大词表采样" -- sampling
+// does not need the softmax row written out.  This kernel therefore reads
+// each row once and writes two numbers per row: HBM traffic is the input
+// alone.
+//
+// Each thread streams its units in tiles.  A tile's maximum (and the first
+// index where it occurs) and its sum of exp(x - max) are folded into the
+// thread's running (m, d, index) with the (m, d) merge, the index following
+// the larger maximum (the earlier one on ties, since a thread visits its
+// elements in increasing order).  Across threads, CTAs and cluster CTAs:
+// the row maximum, then the smallest index holding it, then the sum of
+// d e^(m_t - m).
+#include <cuda_runtime.h>
+
+#include "launch.h"
+
+namespace osr {
+
+constexpr int64_t kNoIndex = 0x7fffffffffffffffLL;
+
+template <int W>
+__device__ __forceinline__ int64_t group_min_i64(int64_t v) {
+#pragma unroll
+    for (int off = W / 2; off > 0; off >>= 1) {
+        const int64_t o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = o < v ? o : v;
+    }
+    return v;
+}
+
+struct MaxArgSum {
+    float m;
+    float d;
+    int64_t i;
+};
+
+template <int W>
+__device__ __forceinline__ MaxArgSum group_mas(MaxArgSum t) {
+    MaxArgSum r;
+    r.m = group_max<W>(t.m);
+    r.i = group_min_i64<W>(t.m == r.m ? t.i : kNoIndex);
+    r.d = group_sum<W>(t.d * expf(t.m - r.m));
+    return r;
+}
+
+template <Dt DI, int G, int U, bool CLUSTER>
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const RowArgs a) {
+    constexpr int NU = kEpt / U;
+    const int64_t nunits = a.N / U;
+    const Slice s = make_slice<G, CLUSTER>(a, nunits);
+    const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+    pdl_wait();
+
+    MaxArgSum t{-FLT_MAX, 0.f, kNoIndex};
+    if (s.ok) {
+        for (int64_t base = s.u0; base < s.u1; base += (int64_t)G * NU) {
+            float v[NU][U];
+#pragma unroll
+            for (int j = 0; j < NU; ++j) {
+                const int64_t ui = base + (int64_t)j * G + s.t;
+                if (ui < s.u1) {
+                    load_unit<DI, U>(xrow, ui * U, v[j]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
+                }
+            }
+            float tm = -FLT_MAX;
+            int64_t ti = kNoIndex;
+#pragma unroll
+            for (int j = 0; j < NU; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (v[j][k] > tm) {
+                        tm = v[j][k];
+                        ti = (base + (int64_t)j * G + s.t) * U + k;
+                    }
+            float td = 0.f;
+#pragma unroll
+            for (int j = 0; j < NU; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], tm);
+            if (tm > t.m) {
+                t.d = t.d * expf(t.m - tm) + td;
+                t.m = tm;
+                t.i = ti;
+            } else {
+                t.d += td * expf(tm - t.m);
+                if (tm == t.m && ti < t.i) t.i = ti;
+            }
+        }
+    }
+
+    MaxArgSum r;
+    if constexpr (G <= 32) {
+        r = group_mas<G>(t);
+    } else {
+        constexpr int NW = RowsGeom<G>::kWarps;
+        __shared__ float s_m[32], s_d[32];
+        __shared__ long long s_i[32];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        float m = group_max<32>(t.m);
+        if (lane == 0) s_m[warp] = m;
+        __syncthreads();
+        m = group_max<NW>(s_m[lane & (NW - 1)]);
+        const int64_t wi = group_min_i64<32>(t.m == m ? t.i : kNoIndex);
+        const float wd = group_sum<32>(t.d * expf(t.m - m));
+        if (lane == 0) {
+            s_d[warp] = wd;
+            s_i[warp] = wi;
+        }
+        __syncthreads();
+        r.m = m;
+        r.d = group_sum<NW>(s_d[lane & (NW - 1)]);
+        r.i = group_min_i64<NW>(s_i[lane & (NW - 1)]);
+    }
+    if constexpr (CLUSTER) {
+        // CTA results through distributed shared memory; every warp reduces
+        // the cs of them (lanes r and r + 16 read CTA r)
+        __shared__ float2 slot_md;
+        __shared__ long long slot_i;
+        if (threadIdx.x == 0) {
+            slot_md = make_float2(r.m, r.d);
+            slot_i = r.i;
+        }
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        const int q = threadIdx.x & 15;
+        MaxArgSum p{-FLT_MAX, 0.f, kNoIndex};
+        if (q < a.cs) {
+            const float2 md = ld_dsmem_f2(mapa_shared(smem_u32(&slot_md), q));
+            long long pi;
+            asm volatile("ld.shared::cluster.s64 %0, [%1];"
+                         : "=l"(pi)
+                         : "r"(mapa_shared(smem_u32(&slot_i), q))
+                         : "memory");
+            p = MaxArgSum{md.x, md.y, pi};
+        }
+        r = group_mas<16>(p);
+        cluster_arrive_relaxed();
+    }
+    if (s.ok && s.t == 0 && s.u0 == 0) {
+        if (a.row_sum != nullptr) a.row_sum[s.row] = r.m + logf(r.d);
+        if (a.row_arg != nullptr) a.row_arg[s.row] = r.i == kNoIndex ? -1 : r.i;
+    }
+    pdl_trigger();
+    if constexpr (CLUSTER) cluster_wait_acquire();
+}
+
+namespace {
+
+using KernelFn = void (*)(RowArgs);
+
+cudaError_t launch_fn(KernelFn k, int64_t grid, int threads, int cs, const RowArgs &a,
+                      cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n++].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
+    if (cs > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cs;
+        attr[n].val.clusterDim.y = 1;
+        attr[n++].val.clusterDim.z = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+template <Dt DI, int U>
+cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cudaStream_t st) {
+    KernelFn fn = nullptr;
+    if (cluster) {
+        if (g == 256) fn = lse_argmax_kernel<DI, 256, U, true>;
+        return fn ? launch_fn(fn, grid, 256, a.cs, a, st) : cudaErrorInvalidConfiguration;
+    }
+#define OSR_MAKE(G) \
+    if (g == G) fn = lse_argmax_kernel<DI, G, U, false>;
+    OSR_MAKE(1) OSR_MAKE(2) OSR_MAKE(4) OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(256)
+#undef OSR_MAKE
+    if (!fn) return cudaErrorInvalidConfiguration;
+    return launch_fn(fn, grid, g <= 32 ? RowsGeom<1>::kThreads : g, 0, a, st);
+}
+
+}  // namespace
+
+template <Dt DI>
+cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t grid,
+                       cudaStream_t st) {
+    if (vec) return launch_lse_u<DI, Elem<DI>::kVec>(a, g, cluster, grid, st);
+    return launch_lse_u<DI, 1>(a, g, cluster, grid, st);
+}
+
+template cudaError_t launch_lse<Dt::F32>(const RowArgs &, int, bool, bool, int64_t, cudaStream_t);
+template cudaError_t launch_lse<Dt::BF16>(const RowArgs &, int, bool, bool, int64_t, cudaStream_t);
+
+}  // namespace osr

@@ -112,13 +112,15 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
             a.row_max[row] = rn.m;
             if (a.row_sum != nullptr) a.row_sum[row] = rn.d;
         }
-        const float inv_d = 1.0f / rn.d;
+        const float inv_d = 1.0f / rn.d, logd = logf(rn.d);
+        const bool logm = (a.flags & kFlagLog) != 0;
         char *yrow = reinterpret_cast<char *>(a.y) + row * a.N * Elem<DO>::kBytes;
         for (int u = threadIdx.x; u < n; u += T) {
             float v[U], o[U];
             lds_unit<DI>(stage + u * 16, v);
 #pragma unroll
-            for (int k = 0; k < U; ++k) o[k] = exp_shifted(v[k], rn.m) * inv_d;
+            for (int k = 0; k < U; ++k)
+                o[k] = logm ? (v[k] - rn.m) - logd : exp_shifted(v[k], rn.m) * inv_d;
             store_unit<DO, U>(yrow, (u0 + u) * U, o);
         }
     }

@@ -67,6 +67,13 @@ cudaError_t softmax_cluster_occupancy(int g, bool vec, int cs, int *n);
 template <Dt D, bool FUSED>
 cudaError_t rmsnorm_cluster_occupancy(int g, bool vec, int cs, int *n);
 
+// Per-row log-sum-exp and argmax (k_lse.cu): g threads per row (g <= 32:
+// 128-thread CTAs of 128/g rows) or 256-thread CTAs; cluster: a.cs CTAs per
+// row over pieces of a.chunk units.  Results go to a.row_sum / a.row_arg.
+template <Dt DI>
+cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t grid,
+                       cudaStream_t st);
+
 // Staged softmax tier (k_staged.cu): grid = rows * a.cs CTAs of
 // kStagedThreads, clusters of a.cs, `smem` bytes of dynamic shared memory.
 template <Dt DI, Dt DO>

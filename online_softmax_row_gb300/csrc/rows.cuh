@@ -31,7 +31,8 @@ struct RowArgs {
     const void *gamma;  // norms: [N] scale
     void *y;            // output rows
     float *row_max;     // softmax statistics, may be null
-    float *row_sum;
+    float *row_sum;     // (the log-sum-exp kernel writes log-sum-exp here)
+    int64_t *row_arg;   // log-sum-exp kernel: index of the row maximum, may be null
     void *ws;           // split tier: per-piece partial states
     int64_t M;          // rows
     int64_t N;          // row length in elements
@@ -45,6 +46,8 @@ struct RowArgs {
 // Test hook: the staged tier's copy barrier gets no arrival, so its bounded
 // wait runs out and the kernel reports a fault instead of computing.
 constexpr int kFlagNoArrive = 1;
+// Softmax kernels: write log-softmax, (x - m) - log d, instead of exp(x - m) / d.
+constexpr int kFlagLog = 2;
 
 template <int G>
 struct RowsGeom {
@@ -118,13 +121,16 @@ softmax_rows_kernel(const RowArgs a) {
     for (int j = 0; j < NU; ++j)
 #pragma unroll
         for (int k = 0; k < U; ++k) mt = fmaxf(mt, v[j][k]);
+    // log-softmax keeps the inputs; softmax replaces them by their exps
+    const bool logm = (a.flags & kFlagLog) != 0;
     float dt = 0.f;
 #pragma unroll
     for (int j = 0; j < NU; ++j)
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            v[j][k] = exp_shifted(v[j][k], mt);
-            dt += v[j][k];
+            const float e = exp_shifted(v[j][k], mt);
+            dt += e;
+            v[j][k] = logm ? v[j][k] : e;
         }
 
     RowNorm rn;
@@ -140,6 +146,7 @@ softmax_rows_kernel(const RowArgs a) {
     }
 
     const float scale = rn.f / rn.d;
+    const float logd = logf(rn.d);
     if (a.row_max != nullptr && s.ok && s.t == 0 && s.u0 == 0) {
         a.row_max[s.row] = rn.m;
         if (a.row_sum != nullptr) a.row_sum[s.row] = rn.d;
@@ -152,7 +159,7 @@ softmax_rows_kernel(const RowArgs a) {
         if (s.ok && ui < s.u1) {
             float o[U];
 #pragma unroll
-            for (int k = 0; k < U; ++k) o[k] = v[j][k] * scale;
+            for (int k = 0; k < U; ++k) o[k] = logm ? (v[j][k] - rn.m) - logd : v[j][k] * scale;
             store_unit<DO, U>(yrow, ui * U, o);
         }
     }

@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a)
         a.row_max[q.row] = st.m;
         if (a.row_sum != nullptr) a.row_sum[q.row] = st.d;
     }
-    const float inv_d = 1.0f / st.d;
+    const float inv_d = 1.0f / st.d, logd = logf(st.d);
+    const bool logm = (a.flags & kFlagLog) != 0;
     const char *xrow = reinterpret_cast<const char *>(a.x) + q.row * a.N * Elem<DI>::kBytes;
     char *yrow = reinterpret_cast<char *>(a.y) + q.row * a.N * Elem<DO>::kBytes;
     for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
@@ -121,7 +122,8 @@ __global__ void __launch_bounds__(G) softmax_split_apply_kernel(const RowArgs a)
             if (ui < q.u1) {
                 float o[U];
 #pragma unroll
-                for (int k = 0; k < U; ++k) o[k] = exp_shifted(v[j][k], st.m) * inv_d;
+                for (int k = 0; k < U; ++k)
+                    o[k] = logm ? (v[j][k] - st.m) - logd : exp_shifted(v[j][k], st.m) * inv_d;
                 store_unit<DO, U>(yrow, ui * U, o);
             }
         }

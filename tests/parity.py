@@ -52,6 +52,19 @@ def check_f32(got: torch.Tensor, ref: np.ndarray, what: str = ""):
     return 0.0
 
 
+def check_f32_abs(got: torch.Tensor, ref: np.ndarray, atol: float, rtol: float, what: str = ""):
+    """|gpu - ref| <= atol + rtol |ref| for every element (NaN matches NaN,
+    equal infinities match)."""
+    g = got.detach().cpu().numpy().astype(np.float64).reshape(ref.shape)
+    same = (np.isnan(g) & np.isnan(ref)) | (g == ref)
+    err = np.abs(g - ref)
+    bad = ~same & ~(err <= atol + rtol * np.abs(ref))
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements outside tolerance; first at {tuple(i)}: "
+                             f"gpu={g[tuple(i)]!r} ref={ref[tuple(i)]!r}")
+
+
 def check_bf16(got: torch.Tensor, ref: np.ndarray, what: str = "", max_ulp: int = 1):
     g = bits16(got).reshape(ref.shape)
     r = oracle.round_to(ref, "bf16")

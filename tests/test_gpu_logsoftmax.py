@@ -1,0 +1,157 @@
+"""Log-softmax and the per-row log-sum-exp / argmax against the fp64 oracle.
+
+Tolerances derived from the binary32 arithmetic (the oracle is exact to
+binary64):
+  log-softmax, binary32 out: |gpu - ref| <= 4e-6 + 1e-5 |ref|.  The result is
+    (x - m) - log d; d carries the rounding of its summation tree (at most
+    ~2.5e-6 relative for the tiers here: 16 sequential terms per thread and
+    <= 26 tree levels), which logf turns into an absolute error of the same
+    size, plus one rounding each for x - m, log and the subtraction.  Values
+    near 0 (a dominant row maximum) are bounded absolutely, not relatively.
+  log-softmax, bf16 out: within 1 bf16 ulp, as for softmax.
+  log-sum-exp: |gpu - ref| <= 4e-6 + 2e-7 |ref| (the same d error, plus the
+    rounding of m + log d to binary32).
+  argmax: exact, the first index of the maximum on ties."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import online_softmax_row_gb300 as osr
+import workloads
+from parity import check_bf16, check_f32_abs, to_oracle_input
+
+pytestmark = pytest.mark.gpu
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    osr.library()
+
+
+def seed_of(*k):
+    return abs(hash(tuple(k))) % (2 ** 31)
+
+
+def case(M, N, dt, seed, sigma=4.0):
+    return workloads.softmax_inputs(M, N, dt, sigma=sigma, shift_rows=M // 3, seed=seed)["x"]
+
+
+def check_log(x_cpu, y):
+    ref = oracle.log_softmax(to_oracle_input(x_cpu).reshape(y.shape[0], -1)).reshape(y.shape)
+    if y.dtype == torch.float32:
+        check_f32_abs(y, ref, 4e-6, 1e-5, "log-softmax")
+    else:
+        check_bf16(y, ref, "log-softmax")
+
+
+def check_lse(x_cpu, lse, am):
+    xo = to_oracle_input(x_cpu).reshape(lse.shape[0], -1)
+    r_lse, r_am = oracle.logsumexp_argmax(xo)
+    assert np.array_equal(am.cpu().numpy(), r_am), "argmax"
+    check_f32_abs(lse, r_lse, 4e-6, 2e-7, "logsumexp")
+
+
+SHAPES = [(1, 1), (5, 3), (4, 33), (9, 128), (33, 1000), (3, 1023), (4, 4096), (2, 8193),
+          (3, 16384), (2, 32768), (1, 152064), (2, 300000)]
+
+
+@pytest.mark.parametrize("io", [("f32", "f32"), ("f32", "bf16"), ("bf16", "f32"), ("bf16", "bf16")])
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_log_softmax(M, N, io):
+    x = case(M, N, io[0], seed_of("log", M, N, io))
+    y = osr.log_softmax_rows(x.cuda(), out_dtype=DT[io[1]])
+    torch.cuda.synchronize()
+    check_log(x, y)
+
+
+@pytest.mark.parametrize("spec", ["rows:g=512", "cluster:g=256,cs=5", "staged:cs=3", "split:s=6,b=4"])
+def test_log_softmax_every_tier(spec):
+    x = case(37, 5000, "f32", seed_of("logtier", spec))
+    os.environ["OSR_FORCE_KERNEL"] = spec
+    try:
+        y = osr.log_softmax_rows(x.cuda())
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["OSR_FORCE_KERNEL"]
+    check_log(x, y)
+
+
+def test_log_softmax_misaligned_and_in_place():
+    x = case(6, 1001, "f32", 3)
+    buf = torch.empty(6 * 1001 + 1, device="cuda")
+    xm = buf[1:].view(6, 1001)
+    xm.copy_(x.cuda())
+    osr.log_softmax_rows(xm, out=xm)
+    torch.cuda.synchronize()
+    check_log(x, xm)
+
+
+def test_log_softmax_minus_inf():
+    x = torch.tensor([[0.0, -float("inf"), 1.0, 2.0]], device="cuda")
+    y = osr.log_softmax_rows(x).cpu()
+    assert y[0, 1] == -float("inf")
+    assert abs(float(torch.logsumexp(y[0, [0, 2, 3]].double(), 0))) < 1e-6
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N", [(1, 1), (7, 2), (100, 32), (33, 1000), (3, 1023), (64, 4096),
+                                 (9, 32768), (4, 152064), (1, 152064), (2, 300000), (300, 5000)])
+def test_row_logsumexp(M, N, dt):
+    x = case(M, N, dt, seed_of("lse", M, N, dt))
+    lse, am = osr.row_logsumexp(x.cuda())
+    torch.cuda.synchronize()
+    check_lse(x, lse, am)
+
+
+def test_row_logsumexp_only_one_output_and_misaligned():
+    x = case(10, 3001, "bf16", 5)
+    buf = torch.empty(10 * 3001 + 1, dtype=torch.bfloat16, device="cuda")
+    xm = buf[1:].view(10, 3001)
+    xm.copy_(x.cuda())
+    lse, am = osr.row_logsumexp(xm, want_argmax=False)
+    assert am is None
+    _, am2 = osr.row_logsumexp(xm, want_lse=False)
+    torch.cuda.synchronize()
+    check_lse(x, lse, am2)
+
+
+def test_row_logsumexp_ties_and_edges():
+    x = torch.tensor([[1.0, 5.0, 5.0, 2.0, 5.0],
+                      [7.0, 7.0, 7.0, 7.0, 7.0],
+                      [-float("inf")] * 5,
+                      [0.0, float("nan"), 3.0, 3.0, 1.0]], device="cuda")
+    lse, am = osr.row_logsumexp(x)
+    lse, am = lse.cpu(), am.cpu()
+    assert am.tolist()[:3] == [1, 0, -1]
+    assert am[3] == 2                                        # NaN is skipped by the maximum
+    assert lse[2] == -float("inf") and torch.isnan(lse[3])
+    assert abs(float(lse[1]) - (7.0 + np.log(5.0))) < 1e-6
+    # ties placed far apart so they fall to different threads and CTAs
+    for N in (4096, 152064):
+        row = torch.zeros(3, N, device="cuda")
+        row[:, 7] = 9.0
+        row[:, N - 5] = 9.0
+        _, am = osr.row_logsumexp(row)
+        assert am.cpu().tolist() == [7, 7, 7]
+
+
+def test_vocab_workload_sampling_statistics():
+    w = workloads.WORKLOADS["logsumexp_argmax_vocab_bf16_64x152064"]
+    x = workloads.make(w)["x"]
+    lse, am = osr.row_logsumexp(x.cuda())
+    torch.cuda.synchronize()
+    check_lse(x, lse, am)
+
+
+def test_log_softmax_vocab_workload_full_size():
+    w = workloads.WORKLOADS["log_softmax_vocab_bf16_f32_64x152064"]
+    x = workloads.make(w)["x"]
+    y = osr.log_softmax_rows(x.cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check_log(x, y)

@@ -24,7 +24,7 @@ ELEM_BYTES = {"f32": 4, "bf16": 2}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "softmax"
+    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "softmax" | "log_softmax" | "logsumexp"
     M: int
     N: int                  # row length (H for the norms)
     in_dtype: str
@@ -49,6 +49,8 @@ class Workload:
             return n * e_in + n * e_out + self.N * e_in
         if self.op == "fused_add_rmsnorm":
             return 2 * n * e_in + 2 * n * e_out + self.N * e_in
+        if self.op == "logsumexp":  # reads the rows, writes a float and an int64 per row
+            return n * e_in + self.M * (4 + 8)
         return n * e_in + n * e_out
 
 
@@ -70,6 +72,14 @@ WORKLOADS = {
         spikes_per_row=8, l2_resident=True,
         note="vocabulary-logit softmax, bf16 in / fp32 out, 64 rows x 152064, 8 spikes +30 per row"),
 }
+WORKLOADS["log_softmax_vocab_bf16_f32_64x152064"] = Workload(
+    "log_softmax_vocab_bf16_f32_64x152064", "log_softmax", 64, 152064, "bf16", "f32", sigma=4.0,
+    spikes_per_row=8, l2_resident=True,
+    note="log-softmax of the vocabulary-logit rows, bf16 in / fp32 out")
+WORKLOADS["logsumexp_argmax_vocab_bf16_64x152064"] = Workload(
+    "logsumexp_argmax_vocab_bf16_64x152064", "logsumexp", 64, 152064, "bf16", "f32", sigma=4.0,
+    spikes_per_row=8, l2_resident=True,
+    note="sampling statistics of the vocabulary-logit rows: log-sum-exp and argmax, no probabilities")
 for _n in SWEEP_N:
     _name = f"softmax_sweep_f32_N{_n}"
     WORKLOADS[_name] = Workload(_name, "softmax", (1 << 26) // _n, _n, "f32", "f32", sigma=2.0,
