@@ -231,7 +231,7 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
 // Log-sum-exp / argmax geometry: the kernel streams, so any shape fits; it
 // only has to spread the rows.  Short rows: a group of g <= 32 lanes per row.
 // Otherwise one 256-thread CTA per row, and when there are fewer rows than
-// two per SM, a cluster of up to 8 CTAs per row (portable size).
+// two per SM, a cluster of up to 16 CTAs per row (about four CTAs per SM).
 struct LsePlan {
     int g = 1;
     int cs = 1;
@@ -243,7 +243,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     LsePlan lp;
     const int u = vec ? vec_elems(in_dt) : 1;
     const int64_t nunits = vec ? N / u : N;
-    const int upt = kEpt / u;
+    const int upt = 32 / u;  // the kernel's 32 elements per thread per tile
     const int g = pow2ceil(cdiv(nunits, upt));
     if (g <= 32) {
         lp.g = g;
@@ -253,10 +253,10 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     lp.g = 256;
     int64_t cs = 1;
     if (M < 2 * (int64_t)sms) {
-        cs = pow2ceil(cdiv(2 * (int64_t)sms, M));
+        cs = pow2ceil(cdiv(4 * (int64_t)sms, M));
         const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
         if (cs > most) cs = most;
-        if (cs > 8) cs = 8;
+        if (cs > 16) cs = 16;
         if (cs < 1) cs = 1;
     }
     lp.cs = (int)cs;

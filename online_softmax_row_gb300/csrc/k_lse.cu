@@ -21,6 +21,9 @@
 namespace osr {
 
 constexpr int64_t kNoIndex = 0x7fffffffffffffffLL;
+// elements per thread per tile: twice the row kernels' 16, so each thread
+// keeps 64 (bf16) to 128 (fp32) bytes of loads in flight in a streaming loop
+constexpr int kLseEpt = 32;
 
 template <int W>
 __device__ __forceinline__ int64_t group_min_i64(int64_t v) {
@@ -49,7 +52,7 @@ __device__ __forceinline__ MaxArgSum group_mas(MaxArgSum t) {
 
 template <Dt DI, int G, int U, bool CLUSTER>
 __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const RowArgs a) {
-    constexpr int NU = kEpt / U;
+    constexpr int NU = kLseEpt / U;
     const int64_t nunits = a.N / U;
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
@@ -181,7 +184,13 @@ cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cu
     KernelFn fn = nullptr;
     if (cluster) {
         if (g == 256) fn = lse_argmax_kernel<DI, 256, U, true>;
-        return fn ? launch_fn(fn, grid, 256, a.cs, a, st) : cudaErrorInvalidConfiguration;
+        if (!fn) return cudaErrorInvalidConfiguration;
+        if (a.cs > 8) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_fn(fn, grid, 256, a.cs, a, st);
     }
 #define OSR_MAKE(G) \
     if (g == G) fn = lse_argmax_kernel<DI, G, U, false>;

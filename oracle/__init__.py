@@ -61,6 +61,9 @@ def _configure(lib):
         lib.orc_softmax_chunked_stats.argtypes = [P, I, I64, I64, I64, P, P]
         lib.orc_log_softmax.argtypes = [P, I, I64, I64, P]
         lib.orc_logsumexp_argmax.argtypes = [P, I, I64, I64, P, P]
+        lib.orc_layernorm.argtypes = [P, P, P, I, D, I64, I64, P, P, P]
+        lib.orc_welford.argtypes = [P, I, I64, I64, P, P, P]
+        lib.orc_chan_merge.argtypes = [D, D, D, D, D, D, P, P, P]
         return lib
 
 
@@ -233,3 +236,36 @@ def logsumexp_argmax(x: np.ndarray):
     am = np.empty(M, dtype=np.int64)
     _load().orc_logsumexp_argmax(_ptr(x), _dt(x), M, N, _ptr(lse), _ptr(am))
     return lse, am
+
+
+def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float,
+              return_stats: bool = False):
+    """Two-pass LayerNorm in binary64; stats are (mean, rstd) per row."""
+    x, gamma, beta = _c(x), _c(gamma), _c(beta)
+    dt = _dt(x)
+    if _dt(gamma) != dt or _dt(beta) != dt:
+        raise TypeError("x, gamma and beta share one storage type")
+    M, H = _rows(x)
+    y = np.empty((M, H), dtype=np.float64)
+    mu = np.empty(M, dtype=np.float64)
+    r = np.empty(M, dtype=np.float64)
+    _load().orc_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), dt, float(eps), M, H, _ptr(y), _ptr(mu),
+                          _ptr(r))
+    return (y, mu, r) if return_stats else y
+
+
+def welford(x: np.ndarray):
+    """Welford's (n, mean, M2) of each row, one element at a time."""
+    x = _c(x)
+    M, N = _rows(x)
+    n, mu, m2 = (np.empty(M, dtype=np.float64) for _ in range(3))
+    _load().orc_welford(_ptr(x), _dt(x), M, N, _ptr(n), _ptr(mu), _ptr(m2))
+    return n, mu, m2
+
+
+def chan_merge(a, b):
+    """Chan's merge of two (n, mean, M2) states."""
+    out = [ctypes.c_double() for _ in range(3)]
+    _load().orc_chan_merge(*(float(v) for v in a), *(float(v) for v in b),
+                           *(ctypes.byref(o) for o in out))
+    return tuple(o.value for o in out)

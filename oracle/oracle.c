@@ -133,6 +133,64 @@ void orc_fused_add_rmsnorm(const void *x, const void *residual, const void *gamm
     }
 }
 
+/* LayerNorm, two-pass definition of [AR] "LayerNorm 与 RMSNorm" and [AZ] 八.2:
+ *   mu = (1/H) sum_j x_j,  var = (1/H) sum_j (x_j - mu)^2,
+ *   y_j = (x_j - mu) / sqrt(var + eps) * gamma_j + beta_j.
+ * mean_out/rstd_out (optional) receive mu and 1/sqrt(var + eps) per row. */
+void orc_layernorm(const void *x, const void *gamma, const void *beta, int dt, double eps,
+                   int64_t M, int64_t H, double *y, double *mean_out, double *rstd_out) {
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        double mu = 0.0;
+        for (int64_t j = 0; j < H; ++j) mu += elem(x, dt, i * H + j);
+        mu /= (double)H;
+        double var = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            const double c = elem(x, dt, i * H + j) - mu;
+            var += c * c;
+        }
+        var /= (double)H;
+        const double r = 1.0 / sqrt(var + eps);
+        for (int64_t j = 0; j < H; ++j)
+            y[i * H + j] = (elem(x, dt, i * H + j) - mu) * r * elem(gamma, dt, j) + elem(beta, dt, j);
+        if (mean_out) mean_out[i] = mu;
+        if (rstd_out) rstd_out[i] = r;
+    }
+}
+
+/* Welford's running (n, mean, M2), one element at a time ([AZ] 八.2):
+ *   n <- n + 1,  delta = x - mean,  mean <- mean + delta / n,
+ *   M2 <- M2 + delta * (x - mean)   (with the updated mean).
+ * Returns the state after all N elements of row i, M2 = sum (x - mean)^2. */
+void orc_welford(const void *x, int dt, int64_t M, int64_t N, double *n_out, double *mean_out,
+                 double *m2_out) {
+    for (int64_t i = 0; i < M; ++i) {
+        double n = 0.0, mean = 0.0, m2 = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            const double v = elem(x, dt, i * N + j);
+            n += 1.0;
+            const double delta = v - mean;
+            mean += delta / n;
+            m2 += delta * (v - mean);
+        }
+        n_out[i] = n;
+        mean_out[i] = mean;
+        m2_out[i] = m2;
+    }
+}
+
+/* Chan et al.'s merge of two (n, mean, M2) states ([AZ] 八.2):
+ *   n = na + nb,  delta = mean_b - mean_a,  mean = mean_a + delta nb / n,
+ *   M2 = M2_a + M2_b + delta^2 na nb / n. */
+void orc_chan_merge(double na, double ma, double qa, double nb, double mb, double qb, double *n,
+                    double *mean, double *m2) {
+    const double nn = na + nb;
+    const double delta = mb - ma;
+    *n = nn;
+    *mean = ma + delta * nb / nn;
+    *m2 = qa + qb + delta * delta * na * nb / nn;
+}
+
 /* Passes 1 and 2 of the three-pass safe softmax of [KJ] "稳定 Softmax" and
  * [AZ] 七.2 for row i: m = max_j x_j (and the first j where it occurs),
  * d = sum_j exp(x_j - m). */

@@ -178,9 +178,9 @@ def test_forced_kernel(monkeypatch):
 
 
 def test_logsumexp_plans_and_validation(lib):
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=16 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8192, 32000, "bf16") == "lse-rows g=256 cs=1 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 100000, 32, "f32") == "lse-rows g=2 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 100000, 32, "f32") == "lse-rows g=1 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOG_SOFTMAX, 64, 4096, "f32") == "rows g=256 ept=16 vec"
     # both outputs NULL, overlapping outputs, NULL input
     assert lib.osr_row_logsumexp(P, None, None, 4, 16, F32, None) == 1

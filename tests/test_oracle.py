@@ -453,3 +453,80 @@ def test_argmax_first_index_on_ties_and_minus_inf():
     assert list(am) == [1, 2, 0]
     ly = oracle.log_softmax(x)
     assert ly[1, 0] == -np.inf and abs(ly[1, 2] + math.log(2)) < 1e-15
+
+
+# --------------------------------------------------------------- LayerNorm, Welford, Chan
+
+def ln_inputs(M, H, lo, hi, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.uniform(lo, hi, (M, H)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    b = rng.standard_normal(H).astype(np.float32)
+    return x, g, b
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 2), (3, 33), (4, 5120)])
+def test_layernorm_matches_torch_fp64(shape, dtype):
+    gen = torch.Generator().manual_seed(shape[1] + 3)
+    x = torch.rand(*shape, generator=gen) * 2 + 100     # mean ~101, the pages' stress case
+    w = torch.rand(shape[1], generator=gen) + 0.5
+    b = torch.randn(shape[1], generator=gen)
+    if dtype == "bf16":
+        x, w, b = x.bfloat16(), w.bfloat16(), b.bfloat16()
+        xa, wa, ba = bf16_bits(x), bf16_bits(w), bf16_bits(b)
+    else:
+        xa, wa, ba = x.numpy(), w.numpy(), b.numpy()
+    y = oracle.layernorm(xa, wa, ba, 1e-5)
+    ref = torch.nn.functional.layer_norm(x.double(), (shape[1],), w.double(), b.double(), 1e-5)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_layernorm_closed_forms():
+    # constant row: x - mu = 0, y = beta
+    H = 9
+    g = np.linspace(0.5, 1.5, H).astype(np.float32)
+    b = np.linspace(-1, 1, H).astype(np.float32)
+    y = oracle.layernorm(np.full(H, 101.25, np.float32), g, b, 1e-5)[0]
+    assert np.array_equal(y, b.astype(np.float64))
+    # two elements a, b: mu = (a+b)/2, var = ((a-b)/2)^2, y = -+s/sqrt(s^2+eps) gamma + beta
+    a, c, eps = 3.0, 7.0, 0.25
+    s_ = (c - a) / 2
+    y, mu, r = oracle.layernorm(f32([a, c]), f32([1, 1]), f32([0, 0]), eps, return_stats=True)
+    assert mu[0] == 5.0 and r[0] == 1 / math.sqrt(s_ * s_ + eps)
+    np.testing.assert_allclose(y[0], [-s_ * r[0], s_ * r[0]], rtol=1e-15)
+
+
+def test_layernorm_standardises_and_is_shift_invariant():
+    x, _, _ = ln_inputs(5, 1000, 100.0, 102.0, 4)
+    ones, zeros = np.ones(1000, np.float32), np.zeros(1000, np.float32)
+    y = oracle.layernorm(x, ones, zeros, 0.0)
+    np.testing.assert_allclose(y.mean(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose((y ** 2).mean(axis=1), 1.0, rtol=1e-12)
+    # on a 2^-10 grid, x - 64 is exact and the output does not move
+    xg = (np.round(x * 1024) / 1024).astype(np.float32)
+    y1 = oracle.layernorm(xg, ones, zeros, 1e-5)
+    y2 = oracle.layernorm((xg.astype(np.float64) - 64.0).astype(np.float32), ones, zeros, 1e-5)
+    np.testing.assert_allclose(y1, y2, rtol=1e-10, atol=1e-10)
+
+
+def test_welford_and_chan_merge_equal_two_pass():
+    x, g, b = ln_inputs(3, 777, 100.0, 102.0, 5)
+    _, mu, r = oracle.layernorm(x, g, b, 0.0, return_stats=True)
+    var = 1 / r ** 2
+    n, wm, m2 = oracle.welford(x)
+    assert np.all(n == 777)
+    np.testing.assert_allclose(wm, mu, rtol=1e-14)
+    np.testing.assert_allclose(m2 / n, var, rtol=1e-10)
+    # random splits merged in random trees (Chan) give the same statistics
+    rnd = random.Random(6)
+    for _ in range(10):
+        cuts = sorted(rnd.sample(range(1, 777), rnd.randint(1, 12)))
+        parts = [oracle.welford(x[0:1, a:b_]) for a, b_ in zip([0] + cuts, cuts + [777])]
+        st = [(p[0][0], p[1][0], p[2][0]) for p in parts]
+        while len(st) > 1:
+            i = rnd.randrange(len(st) - 1)
+            st[i:i + 2] = [oracle.chan_merge(st[i], st[i + 1])]
+        nn, mm, qq = st[0]
+        assert nn == 777 and abs(mm - mu[0]) <= 1e-13 * mu[0]
+        assert abs(qq / nn - var[0]) <= 1e-9 * var[0]

@@ -59,6 +59,18 @@ MUTANTS = [
     ("argmax takes the last index on ties",
      "        if (v > m) {\n            m = v;\n            at = j;",
      "        if (v >= m) {\n            m = v;\n            at = j;"),
+    ("layernorm variance about zero instead of the mean",
+     "const double c = elem(x, dt, i * H + j) - mu;",
+     "const double c = elem(x, dt, i * H + j);"),
+    ("layernorm forgets beta",
+     "* r * elem(gamma, dt, j) + elem(beta, dt, j);",
+     "* r * elem(gamma, dt, j);"),
+    ("welford uses the old mean in the M2 update",
+     "m2 += delta * (v - mean);",
+     "m2 += delta * delta;"),
+    ("chan merge drops the between-group term",
+     "*m2 = qa + qb + delta * delta * na * nb / nn;",
+     "*m2 = qa + qb;"),
     ("chunk summary sums exp without its max",
      "for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - cm);",
      "for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - m);"),
@@ -72,6 +84,7 @@ PARAMS = {
     "test_rmsnorm_matches_torch_rms_norm_fp64": [((5, 33), "f32"), ((5, 33), "bf16")],
     "test_logsumexp_constant_row_closed_form": [(7,)],
     "test_log_softmax_and_logsumexp_match_torch_fp64": [((3, 17),)],
+    "test_layernorm_matches_torch_fp64": [((3, 33), "f32")],
 }
 
 
