@@ -50,7 +50,8 @@ METRIC = "achieved HBM GB/s (min bytes) and % of GB300 HBM peak per kernel, 1 GP
 NOMINAL_HBM_GBS = 8000.0          # NVIDIA's public per-GPU HBM3e figure for GB300
 FALLBACK_HBM_GBS = 6800.0         # used only when no measured peak file exists
 DEFAULT_WORKLOAD = "fused_add_rmsnorm_bf16_8192x4096"
-OP_CODE = {"rmsnorm": 0, "fused_add_rmsnorm": 1, "softmax": 2, "log_softmax": 3, "logsumexp": 4}
+OP_CODE = {"rmsnorm": 0, "fused_add_rmsnorm": 1, "softmax": 2, "log_softmax": 3, "logsumexp": 4,
+           "layernorm": 5}
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -205,6 +206,8 @@ def call(osr, w, s):
         return s["y"]
     if w.op == "rmsnorm":
         return osr.rmsnorm_fwd(s["x"], s["gamma"], w.eps, out=s["y"])
+    if w.op == "layernorm":
+        return osr.layernorm_fwd(s["x"], s["gamma"], s["beta"], w.eps, out=s["y"])
     return osr.fused_add_rmsnorm(s["x"], s["residual"], s["gamma"], w.eps, out=s["y"])
 
 
@@ -375,6 +378,8 @@ def _oracle_inputs(w, rows):
     if w.op in ("softmax", "log_softmax", "logsumexp"):
         inp = workloads.softmax_inputs(rows, w.N, w.in_dtype, w.sigma, 0, w.shift, w.spikes_per_row,
                                        w.spike, seed=0)
+    elif w.op == "layernorm":
+        inp = workloads.layernorm_inputs(rows, w.N, w.in_dtype, w.sigma, w.low, w.high, seed=0)
     else:
         inp = workloads.rmsnorm_inputs(rows, w.N, w.in_dtype, w.sigma, w.op == "fused_add_rmsnorm", seed=0)
     out = {}
@@ -395,6 +400,8 @@ def _run_oracle(oracle, w, inp):
     if w.op == "rmsnorm":
         y = oracle.rmsnorm(inp["x"], inp["gamma"], w.eps)
         return oracle.round_to(y, w.out_dtype)
+    if w.op == "layernorm":
+        return oracle.round_to(oracle.layernorm(inp["x"], inp["gamma"], inp["beta"], w.eps), w.out_dtype)
     h, y = oracle.fused_add_rmsnorm(inp["x"], inp["residual"], inp["gamma"], w.eps)
     return oracle.round_to(h, w.out_dtype), oracle.round_to(y, w.out_dtype)
 

@@ -102,6 +102,19 @@ osr_status osr_fused_add_rmsnorm(const void *x, void *residual, const void *gamm
                                  void *out, int64_t M, int64_t H, osr_dtype dt, void *stream);
 
 /*
+ * LayerNorm forward: y[i, j] = (x[i, j] - mu_i) / sqrt(var_i + eps) * gamma[j]
+ * + beta[j], mu_i = (1/H) sum_j x[i, j], var_i = (1/H) sum_j (x[i, j] - mu_i)^2
+ * ("Softmax 与归一化" (anrans.github.io), "LayerNorm 与 RMSNorm"; "GPU Kernel
+ * 工程（04）" 八.2).  Two passes over the row held on chip, on values shifted
+ * by the row's first element; rows split over CTAs merge their (n, mean, M2)
+ * with Chan's formula.
+ *   x, y [M, H], gamma, beta [H], all of dtype dt; y == x is allowed, any
+ *   other overlap of y with x, gamma or beta -> OSR_ERR_ALIAS.
+ */
+osr_status osr_layernorm_fwd(const void *x, const void *gamma, const void *beta, float eps,
+                             void *y, int64_t M, int64_t H, osr_dtype dt, void *stream);
+
+/*
  * Row softmax: y[i, :] = softmax(x[i, :]).
  *   x  [M, N] dtype in_dt, read only
  *   y  [M, N] dtype out_dt, written
@@ -172,7 +185,7 @@ int osr_last_cuda_error(void);
 /*
  * Which kernel the length-based dispatcher picks, without touching a GPU.
  *   op        0 = RMSNorm, 1 = fused residual-add + RMSNorm, 2 = softmax,
- *             3 = log-softmax, 4 = log-sum-exp / argmax
+ *             3 = log-softmax, 4 = log-sum-exp / argmax, 5 = LayerNorm
  *   vec_ok    1 if every buffer is 16-byte aligned (the 128-bit path)
  *   sm_count  streaming multiprocessors of the target device (152 on GB300)
  *   buf       receives a NUL-terminated description, e.g.

@@ -10,6 +10,7 @@ raises ``OsrError``.
 
 Python name          C entry point
 rmsnorm_fwd          osr_rmsnorm_fwd
+layernorm_fwd        osr_layernorm_fwd
 fused_add_rmsnorm    osr_fused_add_rmsnorm
 softmax_rows         osr_softmax_rows
 softmax_rows_stats   osr_softmax_rows_stats
@@ -29,13 +30,13 @@ import torch
 
 from . import build as _build
 
-__all__ = ["OsrError", "rmsnorm_fwd", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
+__all__ = ["OsrError", "rmsnorm_fwd", "layernorm_fwd", "OP_LAYERNORM", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
            "log_softmax_rows", "row_logsumexp", "OP_LOG_SOFTMAX", "OP_LOGSUMEXP",
            "plan_describe", "bench_copy", "device_fault", "library", "library_path", "OP_RMSNORM",
            "OP_FUSED",
            "OP_SOFTMAX"]
 
-OP_RMSNORM, OP_FUSED, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_LOGSUMEXP = 0, 1, 2, 3, 4
+OP_RMSNORM, OP_FUSED, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_LOGSUMEXP, OP_LAYERNORM = 0, 1, 2, 3, 4, 5
 _DT = {torch.float32: 0, torch.bfloat16: 1}
 _DT_NAME = {"f32": 0, "bf16": 1}
 _STATUS = {0: "OSR_OK", 1: "OSR_ERR_INVALID", 2: "OSR_ERR_ALIGN", 3: "OSR_ERR_ALIAS",
@@ -80,10 +81,12 @@ def library():
         lib.osr_bench_copy.argtypes = [P, P, ctypes.c_size_t, P]
         lib.osr_device_fault.argtypes = [P, ctypes.POINTER(I)]
         lib.osr_log_softmax_rows.argtypes = [P, P, I64, I64, I, I, P]
+        lib.osr_layernorm_fwd.argtypes = [P, P, P, F, P, I64, I64, I, P]
         lib.osr_row_logsumexp.argtypes = [P, P, P, I64, I64, I, P]
         for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
                    "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy",
-                   "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp"):
+                   "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp",
+                   "osr_layernorm_fwd"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -147,6 +150,25 @@ def rmsnorm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
     lib = _lib or library()
     _check(_run(x, lib.osr_rmsnorm_fwd, x.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
                 M, H, _DT[x.dtype]), "osr_rmsnorm_fwd")
+    return out
+
+
+def layernorm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = (x - mean) / sqrt(var + eps) * gamma + beta over the last dimension."""
+    M, H = _rows(x, "x")
+    for name, t in (("gamma", gamma), ("beta", beta)):
+        if t.shape != (H,) or t.dtype != x.dtype:
+            raise OsrError(1, name, f"expected shape ({H},) and dtype {x.dtype}")
+        _rows(t, name)
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype:
+        raise OsrError(1, "out", "shape/dtype must match x")
+    _rows(out, "out")
+    lib = _lib or library()
+    _check(_run(x, lib.osr_layernorm_fwd, x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+                float(eps), out.data_ptr(), M, H, _DT[x.dtype]), "osr_layernorm_fwd")
     return out
 
 

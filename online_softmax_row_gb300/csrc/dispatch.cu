@@ -38,6 +38,12 @@ int vec_elems(osr_dtype d) { return d == OSR_F32 ? 4 : 8; }
 bool dtype_ok(osr_dtype d) { return d == OSR_F32 || d == OSR_BF16; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// elements per thread per tile of an operation's row kernels
+int ept_of(Op op, osr_dtype dt, bool vec) {
+    if (op == Op::Softmax || dt != OSR_BF16 || !vec) return kEpt;
+    return op == Op::FusedAddRmsNorm ? norm_ept<Dt::BF16, 8, true>() : norm_ept<Dt::BF16, 8>();
+}
 int pow2ceil(int64_t v) {
     int p = 1;
     while (p < v) p <<= 1;
@@ -161,7 +167,8 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
     *p = Plan();
     p->vec = vec;
     p->u = vec ? vec_elems(in_dt) : 1;
-    const int upt = kEpt / p->u;
+    p->ept = ept_of(op, in_dt, vec);
+    const int upt = p->ept / p->u;
     const int64_t nunits = vec ? N / p->u : N;
     const int in_bytes = elem_bytes(in_dt);
 
@@ -231,7 +238,8 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
 // Log-sum-exp / argmax geometry: the kernel streams, so any shape fits; it
 // only has to spread the rows.  Short rows: a group of g <= 32 lanes per row.
 // Otherwise one 256-thread CTA per row, and when there are fewer rows than
-// two per SM, a cluster of up to 16 CTAs per row (about four CTAs per SM).
+// two per SM, a cluster of up to 8 CTAs per row (measured: 16-CTA clusters
+// were 70 % slower on 64 vocabulary rows).
 struct LsePlan {
     int g = 1;
     int cs = 1;
@@ -256,7 +264,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
         cs = pow2ceil(cdiv(4 * (int64_t)sms, M));
         const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
         if (cs > most) cs = most;
-        if (cs > 16) cs = 16;
+        if (cs > 8) cs = 8;
         if (cs < 1) cs = 1;
     }
     lp.cs = (int)cs;
@@ -269,14 +277,14 @@ void describe(const Plan &p, char *buf, size_t n) {
     const char *v = p.vec ? "vec" : "scalar";
     switch (p.tier) {
     case Tier::Rows:
-        snprintf(buf, n, "rows g=%d ept=%d %s", p.g, kEpt, v);
+        snprintf(buf, n, "rows g=%d ept=%d %s", p.g, p.ept, v);
         break;
     case Tier::Cluster:
-        snprintf(buf, n, "cluster cs=%d g=%d ept=%d %s", p.cs, p.g, kEpt, v);
+        snprintf(buf, n, "cluster cs=%d g=%d ept=%d %s", p.cs, p.g, p.ept, v);
         break;
     case Tier::Split:
         snprintf(buf, n, "split s=%d b=%lld g=%d ept=%d %s", p.cs, (long long)p.batch_rows, p.g,
-                 kEpt, v);
+                 p.ept, v);
         break;
     case Tier::Staged:
         snprintf(buf, n, "staged cs=%d g=%d piece=%lldB %s", p.cs, p.g, (long long)p.chunk * 16, v);
@@ -297,6 +305,9 @@ cudaError_t launch(Op op, osr_dtype in_dt, osr_dtype out_dt, Kind k, const RowAr
             return launch_softmax<Dt::BF16, Dt::F32>(k, a, p.g, p.vec, grid, st);
         return launch_softmax<Dt::BF16, Dt::BF16>(k, a, p.g, p.vec, grid, st);
     }
+    if (op == Op::LayerNorm)
+        return in_dt == OSR_F32 ? launch_layernorm<Dt::F32>(k, a, p.g, p.vec, grid, st)
+                                : launch_layernorm<Dt::BF16>(k, a, p.g, p.vec, grid, st);
     const bool fused = op == Op::FusedAddRmsNorm;
     if (in_dt == OSR_F32)
         return fused ? launch_rmsnorm<Dt::F32, true>(k, a, p.g, p.vec, grid, st)
@@ -315,6 +326,9 @@ cudaError_t cluster_occupancy(Op op, osr_dtype in_dt, osr_dtype out_dt, const Pl
             return softmax_cluster_occupancy<Dt::BF16, Dt::F32>(p.g, p.vec, p.cs, n);
         return softmax_cluster_occupancy<Dt::BF16, Dt::BF16>(p.g, p.vec, p.cs, n);
     }
+    if (op == Op::LayerNorm)
+        return in_dt == OSR_F32 ? layernorm_cluster_occupancy<Dt::F32>(p.g, p.vec, p.cs, n)
+                                : layernorm_cluster_occupancy<Dt::BF16>(p.g, p.vec, p.cs, n);
     const bool fused = op == Op::FusedAddRmsNorm;
     if (in_dt == OSR_F32)
         return fused ? rmsnorm_cluster_occupancy<Dt::F32, true>(p.g, p.vec, p.cs, n)
@@ -364,7 +378,7 @@ osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_
     }
     if (n > 0) return OSR_OK;
     if (p->forced) return OSR_ERR_UNSUPPORTED;
-    const int upt = kEpt / p->u;
+    const int upt = p->ept / p->u;
     const int64_t nunits = p->vec ? N / p->u : N;
     split_shape(M, N, nunits, upt, elem_bytes(in_dt), di.sms, 0, 0, p);
     return OSR_OK;
@@ -409,7 +423,9 @@ osr_status execute(Op op, osr_dtype in_dt, osr_dtype out_dt, RowArgs a, const Pl
     case Tier::Split: {
         a.cs = p.cs;
         a.chunk = p.chunk;
-        const size_t state = op == Op::Softmax ? sizeof(float2) : sizeof(float);
+        const size_t state = op == Op::Softmax     ? sizeof(float2)
+                             : op == Op::LayerNorm ? sizeof(float4)
+                                                   : sizeof(float);
         void *ws = nullptr;
         if ((e = cudaMallocAsync(&ws, (size_t)M * p.cs * state, st)) != cudaSuccess)
             return cuda_fail(e);
@@ -487,10 +503,10 @@ int osr_version(void) { return 100; }
 
 osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                              int vec_ok, int sm_count, char *buf, size_t buf_len) {
-    if (op < 0 || op > 4 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
+    if (op < 0 || op > 5 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
         sm_count <= 0)
         return OSR_ERR_INVALID;
-    if (op < 2 && in_dt != out_dt) return OSR_ERR_UNSUPPORTED;
+    if ((op < 2 || op == 5) && in_dt != out_dt) return OSR_ERR_UNSUPPORTED;
     osr_status s = check_sizes(M, N);
     if (s != OSR_OK) return s;
     const bool vec = vec_ok && (N % vec_elems(in_dt)) == 0;
@@ -501,7 +517,8 @@ osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_
         return OSR_OK;
     }
     Plan p;
-    s = make_plan(op >= 2 ? Op::Softmax : (Op)op, M, N, in_dt, out_dt, vec, sm_count, 16, &p);
+    const Op o = op == 5 ? Op::LayerNorm : op >= 2 ? Op::Softmax : (Op)op;
+    s = make_plan(o, M, N, in_dt, out_dt, vec, sm_count, 16, &p);
     if (s != OSR_OK) return s;
     describe(p, buf, buf_len);
     return OSR_OK;
@@ -569,6 +586,39 @@ osr_status osr_fused_add_rmsnorm(const void *x, void *residual, const void *gamm
     a.N = H;
     a.eps = eps;
     return execute(Op::FusedAddRmsNorm, dt, dt, a, p, (cudaStream_t)stream);
+}
+
+osr_status osr_layernorm_fwd(const void *x, const void *gamma, const void *beta, float eps,
+                             void *y, int64_t M, int64_t H, osr_dtype dt, void *stream) {
+    osr_status s = check_sizes(M, H);
+    if (s != OSR_OK) return s;
+    if (!dtype_ok(dt)) return OSR_ERR_INVALID;
+    if (M == 0) return OSR_OK;
+    if (!x || !gamma || !beta || !y) return OSR_ERR_INVALID;
+    const int64_t bytes = M * H * elem_bytes(dt), pbytes = H * elem_bytes(dt);
+    if ((y != x && overlaps(x, bytes, y, bytes)) || overlaps(y, bytes, gamma, pbytes) ||
+        overlaps(y, bytes, beta, pbytes))
+        return OSR_ERR_ALIAS;
+    if (!device_accessible(x) || !device_accessible(gamma) || !device_accessible(beta) ||
+        !device_accessible(y))
+        return OSR_ERR_INVALID;
+    DeviceInfo di;
+    if ((s = device_info(&di)) != OSR_OK) return s;
+    const bool vec = aligned16(x) && aligned16(gamma) && aligned16(beta) && aligned16(y) &&
+                     H % vec_elems(dt) == 0;
+    Plan p;
+    if ((s = make_plan(Op::LayerNorm, M, H, dt, dt, vec, di.sms, di.max_cluster, &p)) != OSR_OK)
+        return s;
+    if ((s = check_cluster_plan(Op::LayerNorm, M, H, dt, dt, di, &p)) != OSR_OK) return s;
+    RowArgs a = {};
+    a.x = x;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.y = y;
+    a.M = M;
+    a.N = H;
+    a.eps = eps;
+    return execute(Op::LayerNorm, dt, dt, a, p, (cudaStream_t)stream);
 }
 
 static osr_status softmax_entry(const void *x, void *y, float *row_max, float *row_sum,

@@ -29,6 +29,7 @@ struct RowArgs {
     const void *x;      // input rows
     void *res;          // fused: residual, read and overwritten
     const void *gamma;  // norms: [N] scale
+    const void *beta;   // LayerNorm: [N] shift
     void *y;            // output rows
     float *row_max;     // softmax statistics, may be null
     float *row_sum;     // (the log-sum-exp kernel writes log-sum-exp here)
@@ -292,6 +293,153 @@ rmsnorm_rows_kernel(const RowArgs a) {
                 for (int k = 0; k < U; ++k) o[k] = v[j][k] * r * g[j][k];
                 store_unit<D, U>(yrow, ui * U, o);
             }
+        }
+    }
+    pdl_trigger();
+    if constexpr (CLUSTER) cluster_wait_acquire();
+}
+
+// ============================================================ LayerNorm
+// y = (x - mu) / sqrt(var + eps) * gamma + beta with the two-pass statistics
+// of "Softmax 与归一化" (anrans.github.io), "LayerNorm 与 RMSNorm", and its
+// exercise 1 (two passes over the row cached in registers).  The values are
+// first shifted by a pivot -- the row's first element, the same for every
+// thread and CTA of the row -- so the binary32 sums work on numbers of the
+// row's spread rather than its mean (the mean-101 stress case of that
+// exercise would otherwise lose five digits to the rounding of the mean):
+//   mu_s = (1/H) sum (x - p),  var = (1/H) sum ((x - p) - mu_s)^2,
+//   y = ((x - p) - mu_s) * rsqrt(var + eps) * gamma + beta.
+// Cluster tier: both sums are taken across the cluster's CTAs through
+// distributed shared memory, two exchanges with one barrier each.  (Merging
+// per-thread (n, mean, M2) states with Chan's formula in a single reduction
+// measured 28 % slower: its divisions cost more than the second barrier.)
+__device__ __forceinline__ float cluster_gather_sum(float v, int cs, float *slot) {
+    if (threadIdx.x == 0) *slot = v;
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    const int q = threadIdx.x & 15;
+    float t = 0.f;
+    if (q < cs) {
+        float r;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                     : "=f"(r)
+                     : "r"(mapa_shared(smem_u32(slot), q))
+                     : "memory");
+        t = r;
+    }
+    return group_sum<16>(t);
+}
+
+template <Dt D, int G, int EPT, int U, bool CLUSTER>
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads)
+layernorm_rows_kernel(const RowArgs a) {
+    constexpr bool kPacked = D == Dt::BF16 && U == 8;
+    constexpr int NU = EPT / U;
+    constexpr int NP = kPacked ? NU : 1;
+    constexpr int NF = kPacked ? 1 : NU;
+    const int64_t nunits = a.N / U;
+    const Slice s = make_slice<G, CLUSTER>(a, nunits);
+    const int64_t row_off = s.row * a.N * Elem<D>::kBytes;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    pdl_wait();
+
+    float p = 0.f;  // pivot: x[row][0]
+    if (s.ok) {
+        float t[1];
+        load_unit<D, 1, Hint::Keep>(xrow, 0, t);
+        p = t[0];
+    }
+    // packed rows prefetch gamma and beta before the reductions, so their
+    // latency overlaps them; fp32 rows read them when used
+    uint4 pk[NP], gp[NP], bp[NP];
+    float v[NF][U];
+    uint32_t valid = 0;  // bit j: unit j of this thread exists
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        const bool in = s.ok && ui < s.u1;
+        valid |= in ? 1u << j : 0u;
+        if constexpr (kPacked) {
+            pk[j] = in ? ld16<Hint::Stream>(xrow + ui * 16) : make_uint4(0, 0, 0, 0);
+            gp[j] = in ? ld16<Hint::ReadOnly>(reinterpret_cast<const char *>(a.gamma) + ui * 16)
+                       : make_uint4(0, 0, 0, 0);
+            bp[j] = in ? ld16<Hint::ReadOnly>(reinterpret_cast<const char *>(a.beta) + ui * 16)
+                       : make_uint4(0, 0, 0, 0);
+        } else if (in) {
+            load_unit<D, U>(xrow, ui * U, v[j]);
+        }
+    }
+    // the thread's values, shifted by the pivot, unit by unit
+    auto shifted = [&](int j, float (&f)[U]) {
+        if constexpr (kPacked) {
+            unpack8(pk[j], f);
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) f[k] = v[j][k];
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) f[k] -= p;
+    };
+
+    float s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+        if (valid >> j & 1u) {
+            float f[U];
+            shifted(j, f);
+#pragma unroll
+            for (int k = 0; k < U; ++k) s1 += f[k];
+        }
+    __shared__ float red1[32], red2[32];
+    __shared__ float slot1, slot2;
+    if constexpr (G <= 32) {
+        s1 = group_sum<G>(s1);
+    } else {
+        s1 = block_sum<RowsGeom<G>::kWarps>(s1, red1);
+    }
+    if constexpr (CLUSTER) s1 = cluster_gather_sum(s1, a.cs, &slot1);
+    const float mu = s1 / (float)a.N;
+
+    float s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+        if (valid >> j & 1u) {
+            float f[U];
+            shifted(j, f);
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const float c = f[k] - mu;
+                s2 = fmaf(c, c, s2);
+            }
+        }
+    if constexpr (G <= 32) {
+        s2 = group_sum<G>(s2);
+    } else {
+        s2 = block_sum<RowsGeom<G>::kWarps>(s2, red2);
+    }
+    if constexpr (CLUSTER) {
+        s2 = cluster_gather_sum(s2, a.cs, &slot2);
+        cluster_arrive_relaxed();
+    }
+    const float r = rsqrtf(s2 / (float)a.N + a.eps);
+
+    char *yrow = reinterpret_cast<char *>(a.y) + row_off;
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (valid >> j & 1u) {
+            float f[U], o[U], gg[U], bb[U];
+            shifted(j, f);
+            if constexpr (kPacked) {
+                unpack8(gp[j], gg);
+                unpack8(bp[j], bb);
+            } else {
+                load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, gg);
+                load_unit<D, U, Hint::ReadOnly>(a.beta, ui * U, bb);
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) o[k] = fmaf((f[k] - mu) * r, gg[k], bb[k]);
+            store_unit<D, U>(yrow, ui * U, o);
         }
     }
     pdl_trigger();

@@ -214,4 +214,156 @@ __global__ void __launch_bounds__(G) rmsnorm_split_apply_kernel(const RowArgs a)
     pdl_trigger();
 }
 
+// ------------------------------------------------------------ LayerNorm, split
+// Pass 1: each piece's (n, mean, M2) of the pivot-shifted values (the pivot,
+// x[row][0], is stored with them, so pass 2 never reads x[row][0] after a
+// piece has overwritten it in place): every tile
+// is summarised by its own two passes in registers and folded into the
+// thread's state with Chan's merge ("GPU Kernel 工程（04）" 八.2, Welford and
+// Chan et al.), then the CTA's states are merged in a fixed tree.  Pass 2:
+// every CTA of a row merges the row's S states in the same fixed tree (so all
+// of them normalise with identical statistics) and streams its piece again.
+struct Chan {
+    float n, mean, m2;
+};
+
+__device__ __forceinline__ Chan chan_merge(Chan a, Chan b) {
+    if (a.n == 0.f) return b;
+    if (b.n == 0.f) return a;
+    const float n = a.n + b.n, delta = b.mean - a.mean, fb = b.n / n;
+    return {n, fmaf(delta, fb, a.mean), a.m2 + b.m2 + delta * delta * a.n * fb};
+}
+
+// Merge the CTA's per-thread states; the result is valid in thread 0.
+template <int NW>
+__device__ __forceinline__ Chan block_chan_to_thread0(Chan c, float4 *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Chan o;
+        o.n = __shfl_down_sync(0xffffffffu, c.n, off);
+        o.mean = __shfl_down_sync(0xffffffffu, c.mean, off);
+        o.m2 = __shfl_down_sync(0xffffffffu, c.m2, off);
+        if (lane + off < 32) c = chan_merge(c, o);
+    }
+    if (lane == 0) red[warp] = make_float4(c.n, c.mean, c.m2, 0.f);
+    __syncthreads();
+    if (warp == 0) {
+        c = Chan{0.f, 0.f, 0.f};
+        if (lane < NW) {
+            const float4 q = red[lane];
+            c = Chan{q.x, q.y, q.z};
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            Chan o;
+            o.n = __shfl_down_sync(0xffffffffu, c.n, off);
+            o.mean = __shfl_down_sync(0xffffffffu, c.mean, off);
+            o.m2 = __shfl_down_sync(0xffffffffu, c.m2, off);
+            if (lane + off < 32) c = chan_merge(c, o);
+        }
+    }
+    return c;
+}
+
+template <Dt D, int G, int EPT, int U>
+__global__ void __launch_bounds__(G) layernorm_split_stats_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    const char *xrow = reinterpret_cast<const char *>(a.x) + q.row * a.N * Elem<D>::kBytes;
+    pdl_wait();
+    float p;
+    {
+        float t[1];
+        load_unit<D, 1, Hint::Keep>(xrow, 0, t);
+        p = t[0];
+    }
+    Chan st{0.f, 0.f, 0.f};
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U];
+        int cnt = 0;
+        float s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                load_unit<D, U, Hint::Keep>(xrow, ui * U, v[j]);
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    v[j][k] -= p;
+                    s1 += v[j][k];
+                }
+                cnt += U;
+            }
+        }
+        if (cnt == 0) continue;
+        const float tm = s1 / (float)cnt;
+        float s2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const float c = v[j][k] - tm;
+                    s2 = fmaf(c, c, s2);
+                }
+            }
+        }
+        st = chan_merge(st, Chan{(float)cnt, tm, s2});
+    }
+    __shared__ float4 red[32];
+    st = block_chan_to_thread0<G / 32>(st, red);
+    if (threadIdx.x == 0)
+        reinterpret_cast<float4 *>(a.ws)[q.row * a.cs + q.p] = make_float4(st.n, st.mean, st.m2, p);
+    pdl_trigger();
+}
+
+template <Dt D, int G, int EPT, int U>
+__global__ void __launch_bounds__(G) layernorm_split_apply_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    const int64_t row_off = q.row * a.N * Elem<D>::kBytes;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    pdl_wait();
+    Chan st{0.f, 0.f, 0.f};
+    if (threadIdx.x < a.cs) {
+        const float4 w = reinterpret_cast<const float4 *>(a.ws)[q.row * a.cs + threadIdx.x];
+        st = Chan{w.x, w.y, w.z};
+    }
+    __shared__ float4 red[32];
+    __shared__ float2 stats;
+    st = block_chan_to_thread0<G / 32>(st, red);
+    if (threadIdx.x == 0) stats = make_float2(st.mean, rsqrtf(st.m2 / (float)a.N + a.eps));
+    const float p = reinterpret_cast<const float4 *>(a.ws)[q.row * a.cs].w;  // pass 1's pivot
+    __syncthreads();
+    const float mu = stats.x, r = stats.y;
+    char *yrow = reinterpret_cast<char *>(a.y) + row_off;
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U], g[NU][U], b[NU][U];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                load_unit<D, U>(xrow, ui * U, v[j]);
+                load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, g[j]);
+                load_unit<D, U, Hint::ReadOnly>(a.beta, ui * U, b[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                float o[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) o[k] = fmaf(((v[j][k] - p) - mu) * r, g[j][k], b[j][k]);
+                store_unit<D, U>(yrow, ui * U, o);
+            }
+        }
+    }
+    pdl_trigger();
+}
+
 }  // namespace osr

@@ -124,11 +124,13 @@ def test_dispatch_long_rows_without_staging():
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 32768, "f32", vec_ok=False).startswith("cluster cs=2")
 
 
-def test_dispatch_capacity_counts_cached_fp32_elements():
-    # the register cache holds widened binary32 values, so a bf16 row needs
-    # the same number of threads as an f32 row of the same length
+def test_dispatch_capacity_counts_cached_elements():
+    # softmax widens its cache to binary32: 16 elements a thread for any dtype;
+    # the norms keep 16-byte bf16 rows packed: 32 elements a thread
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32").startswith("rows g=1024")
-    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16").startswith("cluster cs=2")
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "rows g=1024 ept=32 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 65536, "bf16").startswith("cluster cs=2")
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32767, "bf16").startswith("cluster cs=2 g=1024 ept=16 scalar")
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("staged cs=8")
 
 
@@ -140,6 +142,7 @@ def test_dispatch_scalar_path_when_misaligned():
 
 def test_dispatch_norms():
     assert osr.plan_describe(osr.OP_FUSED, 8192, 4096, "bf16") == "rows g=256 ept=16 vec"
+    assert osr.plan_describe(osr.OP_LAYERNORM, 8192, 4096, "bf16") == "rows g=128 ept=32 vec"
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 3584, "f32") == "rows g=256 ept=16 vec"
     with pytest.raises(osr.OsrError):
         osr.plan_describe(osr.OP_RMSNORM, 64, 3584, "f32", "bf16")
@@ -178,7 +181,7 @@ def test_forced_kernel(monkeypatch):
 
 
 def test_logsumexp_plans_and_validation(lib):
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=16 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8192, 32000, "bf16") == "lse-rows g=256 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 100000, 32, "f32") == "lse-rows g=1 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOG_SOFTMAX, 64, 4096, "f32") == "rows g=256 ept=16 vec"
@@ -189,3 +192,14 @@ def test_logsumexp_plans_and_validation(lib):
     assert lib.osr_row_logsumexp(P, P * 8, P * 8 + 4, 4, 16, F32, None) == 3
     assert lib.osr_row_logsumexp(P, P * 8, None, 0, 16, F32, None) == 0
     assert lib.osr_log_softmax_rows(P, P + 4, 4, 16, F32, F32, None) == 3
+
+
+def test_layernorm_plans_and_validation(lib):
+    assert osr.plan_describe(osr.OP_LAYERNORM, 256, 5120, "f32") == "rows g=512 ept=16 vec"
+    assert osr.plan_describe(osr.OP_LAYERNORM, 4, 40000, "f32").startswith("cluster cs=3 g=1024")
+    assert osr.plan_describe(osr.OP_LAYERNORM, 2, 10 ** 6, "f32").startswith("split")
+    f = ctypes.c_float(1e-5)
+    assert lib.osr_layernorm_fwd(P, P * 8, None, f, P * 16, 4, 16, F32, None) == 1   # NULL beta
+    assert lib.osr_layernorm_fwd(P, P * 8, P * 16 + 8, f, P * 16, 4, 16, F32, None) == 3  # y over beta
+    assert lib.osr_layernorm_fwd(P, P * 8, P * 12, f, P + 4, 4, 16, F32, None) == 3      # y over x
+    assert lib.osr_layernorm_fwd(None, None, None, f, None, 0, 16, F32, None) == 0

@@ -24,7 +24,7 @@ ELEM_BYTES = {"f32": 4, "bf16": 2}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "softmax" | "log_softmax" | "logsumexp"
+    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "layernorm" | "softmax" | "log_softmax" | "logsumexp"
     M: int
     N: int                  # row length (H for the norms)
     in_dtype: str
@@ -32,6 +32,8 @@ class Workload:
     sigma: float = 1.0      # std of the normal samples
     eps: float = 1e-6
     shift_rows: int = 0     # rows that get +shift added (softmax overflow check)
+    low: float | None = None    # LayerNorm: x ~ U(low, high) instead of N(0, sigma^2)
+    high: float | None = None
     shift: float = 1000.0
     spikes_per_row: int = 0
     spike: float = 30.0
@@ -47,6 +49,8 @@ class Workload:
         n = self.M * self.N
         if self.op == "rmsnorm":
             return n * e_in + n * e_out + self.N * e_in
+        if self.op == "layernorm":
+            return n * e_in + n * e_out + 2 * self.N * e_in
         if self.op == "fused_add_rmsnorm":
             return 2 * n * e_in + 2 * n * e_out + self.N * e_in
         if self.op == "logsumexp":  # reads the rows, writes a float and an int64 per row
@@ -72,6 +76,13 @@ WORKLOADS = {
         spikes_per_row=8, l2_resident=True,
         note="vocabulary-logit softmax, bf16 in / fp32 out, 64 rows x 152064, 8 spikes +30 per row"),
 }
+WORKLOADS["layernorm_f32_256x5120_mean101"] = Workload(
+    "layernorm_f32_256x5120_mean101", "layernorm", 256, 5120, "f32", "f32", eps=1e-5,
+    low=100.0, high=102.0, l2_resident=True,
+    note="LayerNorm fp32, 256 x 5120, x ~ U(100, 102): mean >> std stress case")
+WORKLOADS["layernorm_bf16_8192x4096"] = Workload(
+    "layernorm_bf16_8192x4096", "layernorm", 8192, 4096, "bf16", "bf16", eps=1e-5, sigma=1.0,
+    note="LayerNorm bf16, 8192 x 4096")
 WORKLOADS["log_softmax_vocab_bf16_f32_64x152064"] = Workload(
     "log_softmax_vocab_bf16_f32_64x152064", "log_softmax", 64, 152064, "bf16", "f32", sigma=4.0,
     spikes_per_row=8, l2_resident=True,
@@ -106,6 +117,18 @@ def rmsnorm_inputs(M, H, dtype="f32", sigma=1.0, fused=False, seed=0, device="cp
     return out
 
 
+def layernorm_inputs(M, H, dtype="f32", sigma=1.0, low=None, high=None, seed=0, device="cpu"):
+    """x ~ N(0, sigma^2) or U(low, high); gamma ~ U(0.5, 1.5); beta ~ N(0, 1)."""
+    g = _gen(device, seed)
+    if low is None:
+        x = torch.randn(M, H, generator=g, device=device, dtype=torch.float32) * sigma
+    else:
+        x = torch.rand(M, H, generator=g, device=device, dtype=torch.float32) * (high - low) + low
+    gamma = torch.rand(H, generator=g, device=device, dtype=torch.float32) + 0.5
+    beta = torch.randn(H, generator=g, device=device, dtype=torch.float32)
+    return {"x": x.to(_DT[dtype]), "gamma": gamma.to(_DT[dtype]), "beta": beta.to(_DT[dtype])}
+
+
 def softmax_inputs(M, N, dtype="f32", sigma=1.0, shift_rows=0, shift=1000.0,
                    spikes_per_row=0, spike=30.0, seed=0, device="cpu"):
     """x ~ N(0, sigma^2); `shift_rows` distinct rows (seeded permutation) get
@@ -126,6 +149,8 @@ def make(w: Workload | str, seed=0, device="cpu"):
     """Inputs of a named workload, as torch tensors on `device`."""
     if isinstance(w, str):
         w = WORKLOADS[w]
+    if w.op == "layernorm":
+        return layernorm_inputs(w.M, w.N, w.in_dtype, w.sigma, w.low, w.high, seed, device)
     if w.op in ("rmsnorm", "fused_add_rmsnorm"):
         return rmsnorm_inputs(w.M, w.N, w.in_dtype, w.sigma, w.op == "fused_add_rmsnorm",
                               seed, device)
