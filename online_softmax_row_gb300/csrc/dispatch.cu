@@ -41,7 +41,8 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // elements per thread per tile of an operation's row kernels
 int ept_of(Op op, osr_dtype dt, bool vec) {
-    if (op == Op::Softmax || dt != OSR_BF16 || !vec) return kEpt;
+    if (dt != OSR_BF16 || !vec) return kEpt;
+    if (op == Op::Softmax) return softmax_ept<Dt::BF16, 8>();
     return op == Op::FusedAddRmsNorm ? norm_ept<Dt::BF16, 8, true>() : norm_ept<Dt::BF16, 8>();
 }
 int pow2ceil(int64_t v) {
@@ -139,8 +140,10 @@ bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, int64_t f
     return true;
 }
 
-void split_shape(int64_t M, int64_t N, int64_t nunits, int upt, int in_bytes, int sms,
+void split_shape(Op op, int64_t M, int64_t N, int64_t nunits, int in_bytes, int sms,
                  int64_t force_s, int64_t force_b, Plan *p) {
+    if (op == Op::Softmax) p->ept = kEpt;  // the split softmax kernels' tile
+    const int upt = p->ept / p->u;
     const int64_t row_bytes = N * in_bytes;
     int64_t b = force_b > 0 ? force_b : kL2BudgetBytes / (row_bytes > 0 ? row_bytes : 1);
     if (b < 1) b = 1;
@@ -205,15 +208,19 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
             parse_kv(force, "s", &s);
             parse_kv(force, "b", &b);
             if (s > kMaxPieces) return OSR_ERR_UNSUPPORTED;
-            split_shape(M, N, nunits, upt, in_bytes, sms, s, b, p);
+            split_shape(op, M, N, nunits, in_bytes, sms, s, b, p);
             return OSR_OK;
         }
         return OSR_ERR_UNSUPPORTED;
     }
 
-    // 1. the whole row in one group or CTA, register-cached
+    // 1. the whole row in one group or CTA, register-cached.  Softmax with 32
+    //    elements a thread stops at 512 threads: its 1024-thread CTA needs 59-63
+    //    registers (one CTA per SM) and measured 7-25 % slower than staging
+    //    the 64 KiB row in two CTAs' shared memory.
     const int g = pow2ceil(cdiv(nunits, upt));
-    if (g <= 1024) {
+    const int gmax = op == Op::Softmax && p->ept > kEpt && vec ? 512 : 1024;
+    if (g <= gmax) {
         p->tier = Tier::Rows;
         p->g = g;
         return OSR_OK;
@@ -231,7 +238,7 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
         return OSR_OK;
     }
     // 4. two passes through a workspace
-    split_shape(M, N, nunits, upt, in_bytes, sms, 0, 0, p);
+    split_shape(op, M, N, nunits, in_bytes, sms, 0, 0, p);
     return OSR_OK;
 }
 
@@ -378,9 +385,8 @@ osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_
     }
     if (n > 0) return OSR_OK;
     if (p->forced) return OSR_ERR_UNSUPPORTED;
-    const int upt = p->ept / p->u;
     const int64_t nunits = p->vec ? N / p->u : N;
-    split_shape(M, N, nunits, upt, elem_bytes(in_dt), di.sms, 0, 0, p);
+    split_shape(op, M, N, nunits, elem_bytes(in_dt), di.sms, 0, 0, p);
     return OSR_OK;
 }
 

@@ -31,6 +31,14 @@ template <Dt D, int U, bool FUSED = false>
 constexpr int norm_ept() {
     return D == Dt::BF16 && U == 8 && !FUSED ? 32 : 16;
 }
+// Softmax on 16-byte bfloat16 rows: 32 elements per thread in the register
+// tiers, so a thread keeps 64 bytes of loads in flight like the fp32 kernels
+// (the cached values are fp32 either way).  The split-row kernels stay at 16:
+// at 32 the pass-2 kernel needs 99 registers, one 512-thread CTA per SM.
+template <Dt DI, int U>
+constexpr int softmax_ept() {
+    return DI == Dt::BF16 && U == 8 ? 32 : 16;
+}
 constexpr int kSplitThreads = 512;  // threads per split-row CTA
 constexpr int kMaxPieces = kSplitThreads;
 constexpr int kStagedThreads = 256;               // threads per staged CTA

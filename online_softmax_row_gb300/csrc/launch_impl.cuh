@@ -79,13 +79,13 @@ cudaError_t launch_softmax_u(Kind k, const RowArgs &a, int g, int64_t grid, cuda
     switch (k) {
     case Kind::Rows:
 #define OSR_MAKE(G) \
-    if (g == G) { fn = softmax_rows_kernel<DI, DO, G, kEpt, U, false>; threads = RowsGeom<G>::kThreads; }
+    if (g == G) { fn = softmax_rows_kernel<DI, DO, G, softmax_ept<DI, U>(), U, false>; threads = RowsGeom<G>::kThreads; }
         OSR_ROWS_G_CASES(OSR_MAKE)
 #undef OSR_MAKE
         return fn ? launch_plain(fn, grid, threads, a, st) : cudaErrorInvalidConfiguration;
     case Kind::Cluster:
 #define OSR_MAKE(G) \
-    if (g == G) fn = softmax_rows_kernel<DI, DO, G, kEpt, U, true>;
+    if (g == G) fn = softmax_rows_kernel<DI, DO, G, softmax_ept<DI, U>(), U, true>;
         OSR_CLUSTER_G_CASES(OSR_MAKE)
 #undef OSR_MAKE
         return fn ? launch_clustered(fn, grid, g, a.cs, a, st) : cudaErrorInvalidConfiguration;
@@ -110,7 +110,7 @@ template <Dt DI, Dt DO, int U>
 cudaError_t softmax_cluster_occupancy_u(int g, int cs, int *n) {
     KernelFn fn = nullptr;
 #define OSR_MAKE(G) \
-    if (g == G) fn = softmax_rows_kernel<DI, DO, G, kEpt, U, true>;
+    if (g == G) fn = softmax_rows_kernel<DI, DO, G, softmax_ept<DI, U>(), U, true>;
     OSR_CLUSTER_G_CASES(OSR_MAKE)
 #undef OSR_MAKE
     return fn ? cluster_occupancy(fn, g, cs, n) : cudaErrorInvalidConfiguration;

@@ -116,7 +116,7 @@ extern "C" osr_status osr_softmax_rows_noalloc(const void *x, void *y, int64_t M
     const bool vec = ((uintptr_t)x % 16 == 0) && ((uintptr_t)y % 16 == 0) && (N % vecn == 0);
     const int u = vec ? vecn : 1;
     const int64_t nunits = vec ? N / u : N;
-    const int upt = osr::kEpt / u;
+    const int upt = osr::kEpt / u;  // the split softmax kernels' tile
     int64_t b = (48ll << 20) / (N * in_b);
     if (b < 1) b = 1;
     if (b > M) b = M;

@@ -125,9 +125,13 @@ def test_dispatch_long_rows_without_staging():
 
 
 def test_dispatch_capacity_counts_cached_elements():
-    # softmax widens its cache to binary32: 16 elements a thread for any dtype;
-    # the norms keep 16-byte bf16 rows packed: 32 elements a thread
-    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32").startswith("rows g=1024")
+    # 16-byte bf16 rows: 32 elements a thread (softmax caches them as binary32,
+    # the norms keep them packed); the split softmax kernels stay at 16
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32") == "rows g=512 ept=32 vec"
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "f32") == "rows g=1024 ept=16 vec"
+    assert osr.plan_describe(osr.OP_SOFTMAX, 2048, 32768, "bf16", "f32").startswith("staged cs=2")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32").startswith("split")
+    assert "ept=16" in osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32")
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "rows g=1024 ept=32 vec"
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 65536, "bf16").startswith("cluster cs=2")
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 32767, "bf16").startswith("cluster cs=2 g=1024 ept=16 scalar")

@@ -9,7 +9,9 @@ Recipe (every workload): one ``torch.Generator`` seeded with ``seed``
 (default 0) on the requested device; binary32 samples are drawn in the order
 x, residual, gamma, then the structure (shifted rows, spike columns); the cast
 to bfloat16 (round-to-nearest-even) comes last.  Shapes follow the Qwen2.5-7B
-numbers the pages use (hidden 3584, 28 heads, vocabulary 152064).
+numbers the pages use (hidden 3584, 28 heads, vocabulary 152064, scored
+context 2048).  Masks are structure: entries set to -inf after sampling
+(causal: key j > query i; keep-K: all but K seeded columns per row).
 """
 from __future__ import annotations
 
@@ -37,6 +39,7 @@ class Workload:
     shift: float = 1000.0
     spikes_per_row: int = 0
     spike: float = 30.0
+    mask: str = ""          # "" | "causal" (square per head: query = row % N) | "keep:K"
     l2_resident: bool = False
     note: str = ""
     extra: dict = field(default_factory=dict)
@@ -91,6 +94,31 @@ WORKLOADS["logsumexp_argmax_vocab_bf16_64x152064"] = Workload(
     "logsumexp_argmax_vocab_bf16_64x152064", "logsumexp", 64, 152064, "bf16", "f32", sigma=4.0,
     spikes_per_row=8, l2_resident=True,
     note="sampling statistics of the vocabulary-logit rows: log-sum-exp and argmax, no probabilities")
+WORKLOADS["softmax_causal_f32_57344x2048"] = Workload(
+    "softmax_causal_f32_57344x2048", "softmax", 28 * 2048, 2048, "f32", "f32", sigma=3.0,
+    mask="causal",
+    note="causally masked attention-score softmax fp32, 28 heads x 2048 queries x 2048 keys: "
+         "key j > query i is -inf (half the entries)")
+WORKLOADS["softmax_topk_masked_bf16_f32_64x152064"] = Workload(
+    "softmax_topk_masked_bf16_f32_64x152064", "softmax", 64, 152064, "bf16", "f32", sigma=4.0,
+    mask="keep:64", l2_resident=True,
+    note="vocabulary rows after a top-k style filter: all but 64 seeded columns per row are -inf")
+WORKLOADS["softmax_attn_bf16_114688x4096"] = Workload(
+    "softmax_attn_bf16_114688x4096", "softmax", 28 * 4096, 4096, "bf16", "bf16", sigma=3.0,
+    shift_rows=round(0.01 * 28 * 4096),
+    note="attention-score softmax with bf16 output, 28 heads x 4096 x 4096, 1% rows +1000")
+# the pages' shape sweep: decode batch 1 and 32, a 2048-token prefill, a 16384-row batch
+SHAPE_SWEEP_M = (1, 32, 2048, 16384)
+for _m in SHAPE_SWEEP_M:
+    _name = f"shape_rmsnorm_f32_{_m}x3584"
+    WORKLOADS[_name] = Workload(_name, "rmsnorm", _m, 3584, "f32", "f32", sigma=1.0,
+                                l2_resident=_m * 3584 * 8 < (64 << 20),
+                                note=f"RMSNorm fp32 shape sweep, M={_m}, hidden 3584")
+for _m in SHAPE_SWEEP_M:
+    _name = f"shape_softmax_f32_{_m}x2048"
+    WORKLOADS[_name] = Workload(_name, "softmax", _m, 2048, "f32", "f32", sigma=3.0,
+                                l2_resident=_m * 2048 * 8 < (64 << 20),
+                                note=f"score softmax fp32 shape sweep, M={_m}, context 2048")
 for _n in SWEEP_N:
     _name = f"softmax_sweep_f32_N{_n}"
     WORKLOADS[_name] = Workload(_name, "softmax", (1 << 26) // _n, _n, "f32", "f32", sigma=2.0,
@@ -130,9 +158,12 @@ def layernorm_inputs(M, H, dtype="f32", sigma=1.0, low=None, high=None, seed=0, 
 
 
 def softmax_inputs(M, N, dtype="f32", sigma=1.0, shift_rows=0, shift=1000.0,
-                   spikes_per_row=0, spike=30.0, seed=0, device="cpu"):
+                   spikes_per_row=0, spike=30.0, seed=0, device="cpu", mask=""):
     """x ~ N(0, sigma^2); `shift_rows` distinct rows (seeded permutation) get
-    +shift; each row gets `spikes_per_row` distinct seeded columns +spike."""
+    +shift; each row gets `spikes_per_row` distinct seeded columns +spike;
+    then `mask` sets entries to -inf: "causal" masks key j > query i, the
+    query of row r being r mod N (square score blocks per head); "keep:K"
+    keeps K distinct seeded columns of each row and masks the rest."""
     g = _gen(device, seed)
     x = torch.randn(M, N, generator=g, device=device, dtype=torch.float32) * sigma
     if shift_rows:
@@ -142,6 +173,17 @@ def softmax_inputs(M, N, dtype="f32", sigma=1.0, shift_rows=0, shift=1000.0,
         for r in range(M):
             cols = torch.randperm(N, generator=g, device=device)[:spikes_per_row]
             x[r, cols] += spike
+    if mask == "causal":
+        q = (torch.arange(M, device=device) % N).unsqueeze(1)
+        x.masked_fill_(torch.arange(N, device=device).unsqueeze(0) > q, float("-inf"))
+    elif mask.startswith("keep:"):
+        k = int(mask.split(":")[1])
+        keep = torch.rand(M, N, generator=g, device=device).argsort(dim=1)[:, :k]
+        masked = torch.full_like(x, float("-inf"))
+        masked.scatter_(1, keep, x.gather(1, keep))
+        x = masked
+    elif mask:
+        raise ValueError(f"unknown mask {mask!r}")
     return {"x": x.to(_DT[dtype])}
 
 
@@ -155,4 +197,4 @@ def make(w: Workload | str, seed=0, device="cpu"):
         return rmsnorm_inputs(w.M, w.N, w.in_dtype, w.sigma, w.op == "fused_add_rmsnorm",
                               seed, device)
     return softmax_inputs(w.M, w.N, w.in_dtype, w.sigma, w.shift_rows, w.shift,
-                          w.spikes_per_row, w.spike, seed, device)
+                          w.spikes_per_row, w.spike, seed, device, w.mask)
