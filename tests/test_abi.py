@@ -129,7 +129,7 @@ def test_dispatch_capacity_counts_cached_elements():
     # the norms keep them packed); the split softmax kernels stay at 16
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32") == "rows g=512 ept=32 vec"
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "f32") == "rows g=1024 ept=16 vec"
-    assert osr.plan_describe(osr.OP_SOFTMAX, 2048, 32768, "bf16", "f32").startswith("staged cs=2")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 2048, 32768, "bf16", "f32").startswith("staged cs=1 g=256 piece=65536B")
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32").startswith("split")
     assert "ept=16" in osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32")
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "rows g=1024 ept=32 vec"
