@@ -87,29 +87,57 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash() -> str:
+CSRC = os.path.join(ROOT, "online_softmax_row_gb300", "csrc")
+
+
+def kernel_units(w) -> list[str]:
+    """The translation units whose kernels a call of workload w can run."""
+    d = {"f32": "f", "bf16": "b"}
+    if w.op in ("softmax", "log_softmax"):
+        return [f"k_softmax_{d[w.in_dtype]}{d[w.out_dtype]}.cu", "k_staged.cu"]
+    if w.op == "logsumexp":
+        return ["k_lse.cu"]
+    prefix = {"rmsnorm": "k_rms", "fused_add_rmsnorm": "k_fused", "layernorm": "k_ln"}[w.op]
+    return [f"{prefix}_{d[w.in_dtype]}.cu"]
+
+
+def _include_closure(paths):
+    seen, todo = set(), [os.path.normpath(p) for p in paths]
+    while todo:
+        p = todo.pop()
+        # kernel sources only: the public C header declares, it compiles no kernel
+        if p in seen or not os.path.exists(p) or os.path.dirname(p) != CSRC:
+            continue
+        seen.add(p)
+        for inc in re.findall(r'^#include "([^"]+)"', open(p, encoding="utf-8").read(), re.M):
+            todo.append(os.path.normpath(os.path.join(os.path.dirname(p), inc)))
+    return sorted(seen)
+
+
+def source_hash(w) -> str:
+    """Hash of the sources the workload's kernels are compiled from (their
+    translation units and the kernel headers those include)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "online_softmax_row_gb300", "csrc", "*")))
-    for f in files:
+    for f in _include_closure([os.path.join(CSRC, u) for u in kernel_units(w)]):
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(w, plan: str):
     """Per-launch DRAM bytes of the workload's kernel from the committed ncu
     summary (profiles/dram_traffic.md), if it was captured on the current
-    kernel sources; else None."""
+    sources of that kernel and with the same plan; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     if not os.path.exists(path):
         return None
-    want = source_hash()
+    want = source_hash(w)
     for line in open(path, encoding="utf-8"):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == workload and cells[1] == want:
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 5 and cells[0] == w.name and cells[1] == want and cells[2] == plan:
             try:
-                return int(cells[3].replace(",", ""))
+                return int(cells[4].replace(",", ""))
             except ValueError:
                 return None
     return None
@@ -436,6 +464,11 @@ def ours(args):
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
     peak, peak_src = measured_peaks()
     w = workloads.WORKLOADS[args.workload]
+    if args.max_rows and w.M > args.max_rows:
+        # profiling a smaller case of the same kernel (same row length, plan
+        # and per-row work): traffic then scales by rows
+        w = dataclasses.replace(w, M=args.max_rows,
+                                shift_rows=round(w.shift_rows * args.max_rows / w.M))
     osr.library()
     plan = osr.plan_describe(OP_CODE[w.op], w.M, w.N, w.in_dtype, w.out_dtype, True,
                              props.multi_processor_count)
@@ -455,10 +488,12 @@ def ours(args):
         "dtype": "bf16" if w.in_dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
                    "out_dtype": w.out_dtype, "min_bytes_per_step": w.min_bytes, "kernel": plan,
+                   "rows_capped": bool(args.max_rows and w.M == args.max_rows),
                    "l2": f"rotating {n_sets_for(w, l2)} input/output sets (> 2x L2 of traffic "
                          f"between reuses); no flush", "parallelism": f"rows; {world} GPU(s), weak"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w, plan),
+                     "kernel_source_hash": source_hash(w),
                      "peak_source": peak_src + " -- of measured" if "measured" in peak_src else peak_src,
                      "algorithmic_bytes_per_launch": w.min_bytes // launches_per_call(plan, w.M)},
         "gpu_launches": args.steps * launches_per_call(plan, w.M),
@@ -480,7 +515,7 @@ def ours(args):
                           "frac_measured": round(g / peak, 4), "frac_nominal": round(g / NOMINAL_HBM_GBS, 4),
                           "frac_copy_same_run": round(g / result["peaks"]["copy_kernel_same_run_gbs"], 4),
                           "launches_per_call": launches_per_call(p, wl.M),
-                          "traffic": profiled_traffic(name)})
+                          "traffic": profiled_traffic(wl, p)})
         result["per_kernel"] = suite
     if rank == 0:
         if not args.profile:
@@ -540,7 +575,12 @@ def main(argv=None):
     ap.add_argument("--profile", action="store_true",
                     help="only the timed steps of the workload (for ncu captures): no clock "
                          "sampling, per-workload table, e2e or CPU baseline")
+    ap.add_argument("--max-rows", type=int, default=0,
+                    help="with --profile: run only the first MAX_ROWS rows of the workload "
+                         "(a capture-sized case of the same kernel)")
     args = ap.parse_args(argv)
+    if args.max_rows and not args.profile:
+        ap.error("--max-rows is for profiling captures only (--profile)")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

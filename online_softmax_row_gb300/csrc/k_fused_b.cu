@@ -1,5 +1,5 @@
 // RMSNorm kernels, storage BF16, fused residual-add: true.
-#include "launch_impl.cuh"
+#include "launch_rmsnorm.cuh"
 
 namespace osr {
 template cudaError_t launch_rmsnorm<Dt::BF16, true>(Kind, const RowArgs &, int, bool, int64_t,

@@ -1,5 +1,5 @@
 // LayerNorm kernels, storage BF16.
-#include "launch_impl.cuh"
+#include "launch_layernorm.cuh"
 
 namespace osr {
 template cudaError_t launch_layernorm<Dt::BF16>(Kind, const RowArgs &, int, bool, int64_t,

@@ -1,5 +1,5 @@
 // Softmax kernels, input F32 / output F32.
-#include "launch_impl.cuh"
+#include "launch_softmax.cuh"
 
 namespace osr {
 template cudaError_t launch_softmax<Dt::F32, Dt::F32>(Kind, const RowArgs &, int, bool, int64_t,

@@ -6,7 +6,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
-#include "rows.cuh"
+#include "row_common.cuh"
 
 namespace osr {
 

@@ -1,0 +1,308 @@
+// layernorm_kernels.cuh -- LayerNorm kernels: the register-cached row/cluster kernel and the two
+// split-row passes.
+#pragma once
+
+#include "row_common.cuh"
+
+namespace osr {
+
+// ============================================================ LayerNorm
+// y = (x - mu) / sqrt(var + eps) * gamma + beta with the two-pass statistics
+// of "Softmax 与归一化" (anrans.github.io), "LayerNorm 与 RMSNorm", and its
+// exercise 1 (two passes over the row cached in registers).  The values are
+// first shifted by a pivot -- the row's first element, the same for every
+// thread and CTA of the row -- so the binary32 sums work on numbers of the
+// row's spread rather than its mean (the mean-101 stress case of that
+// exercise would otherwise lose five digits to the rounding of the mean):
+//   mu_s = (1/H) sum (x - p),  var = (1/H) sum ((x - p) - mu_s)^2,
+//   y = ((x - p) - mu_s) * rsqrt(var + eps) * gamma + beta.
+// Cluster tier: both sums are taken across the cluster's CTAs through
+// distributed shared memory, two exchanges with one barrier each.  (Merging
+// per-thread (n, mean, M2) states with Chan's formula in a single reduction
+// measured 28 % slower: its divisions cost more than the second barrier.)
+__device__ __forceinline__ float cluster_gather_sum(float v, int cs, float *slot) {
+    if (threadIdx.x == 0) *slot = v;
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    const int q = threadIdx.x & 15;
+    float t = 0.f;
+    if (q < cs) {
+        float r;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                     : "=f"(r)
+                     : "r"(mapa_shared(smem_u32(slot), q))
+                     : "memory");
+        t = r;
+    }
+    return group_sum<16>(t);
+}
+
+template <Dt D, int G, int EPT, int U, bool CLUSTER>
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads)
+layernorm_rows_kernel(const RowArgs a) {
+    constexpr bool kPacked = D == Dt::BF16 && U == 8;
+    constexpr int NU = EPT / U;
+    constexpr int NP = kPacked ? NU : 1;
+    constexpr int NF = kPacked ? 1 : NU;
+    const int64_t nunits = a.N / U;
+    const Slice s = make_slice<G, CLUSTER>(a, nunits);
+    const int64_t row_off = s.row * a.N * Elem<D>::kBytes;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    pdl_wait();
+
+    float p = 0.f;  // pivot: x[row][0]
+    if (s.ok) {
+        float t[1];
+        load_unit<D, 1, Hint::Keep>(xrow, 0, t);
+        p = t[0];
+    }
+    // packed rows prefetch gamma and beta before the reductions, so their
+    // latency overlaps them; fp32 rows read them when used
+    uint4 pk[NP], gp[NP], bp[NP];
+    float v[NF][U];
+    uint32_t valid = 0;  // bit j: unit j of this thread exists
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        const bool in = s.ok && ui < s.u1;
+        valid |= in ? 1u << j : 0u;
+        if constexpr (kPacked) {
+            pk[j] = in ? ld16<Hint::Stream>(xrow + ui * 16) : make_uint4(0, 0, 0, 0);
+            gp[j] = in ? ld16<Hint::ReadOnly>(reinterpret_cast<const char *>(a.gamma) + ui * 16)
+                       : make_uint4(0, 0, 0, 0);
+            bp[j] = in ? ld16<Hint::ReadOnly>(reinterpret_cast<const char *>(a.beta) + ui * 16)
+                       : make_uint4(0, 0, 0, 0);
+        } else if (in) {
+            load_unit<D, U>(xrow, ui * U, v[j]);
+        }
+    }
+    // the thread's values, shifted by the pivot, unit by unit
+    auto shifted = [&](int j, float (&f)[U]) {
+        if constexpr (kPacked) {
+            unpack8(pk[j], f);
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) f[k] = v[j][k];
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) f[k] -= p;
+    };
+
+    float s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+        if (valid >> j & 1u) {
+            float f[U];
+            shifted(j, f);
+#pragma unroll
+            for (int k = 0; k < U; ++k) s1 += f[k];
+        }
+    __shared__ float red1[32], red2[32];
+    __shared__ float slot1, slot2;
+    if constexpr (G <= 32) {
+        s1 = group_sum<G>(s1);
+    } else {
+        s1 = block_sum<RowsGeom<G>::kWarps>(s1, red1);
+    }
+    if constexpr (CLUSTER) s1 = cluster_gather_sum(s1, a.cs, &slot1);
+    const float mu = s1 / (float)a.N;
+
+    float s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NU; ++j)
+        if (valid >> j & 1u) {
+            float f[U];
+            shifted(j, f);
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const float c = f[k] - mu;
+                s2 = fmaf(c, c, s2);
+            }
+        }
+    if constexpr (G <= 32) {
+        s2 = group_sum<G>(s2);
+    } else {
+        s2 = block_sum<RowsGeom<G>::kWarps>(s2, red2);
+    }
+    if constexpr (CLUSTER) {
+        s2 = cluster_gather_sum(s2, a.cs, &slot2);
+        cluster_arrive_relaxed();
+    }
+    const float r = rsqrtf(s2 / (float)a.N + a.eps);
+
+    char *yrow = reinterpret_cast<char *>(a.y) + row_off;
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+        if (valid >> j & 1u) {
+            float f[U], o[U], gg[U], bb[U];
+            shifted(j, f);
+            if constexpr (kPacked) {
+                unpack8(gp[j], gg);
+                unpack8(bp[j], bb);
+            } else {
+                load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, gg);
+                load_unit<D, U, Hint::ReadOnly>(a.beta, ui * U, bb);
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) o[k] = fmaf((f[k] - mu) * r, gg[k], bb[k]);
+            store_unit<D, U>(yrow, ui * U, o);
+        }
+    }
+    pdl_trigger();
+    if constexpr (CLUSTER) cluster_wait_acquire();
+}
+
+// ------------------------------------------------------------ LayerNorm, split
+// Pass 1: each piece's (n, mean, M2) of the pivot-shifted values (the pivot,
+// x[row][0], is stored with them, so pass 2 never reads x[row][0] after a
+// piece has overwritten it in place): every tile
+// is summarised by its own two passes in registers and folded into the
+// thread's state with Chan's merge ("GPU Kernel 工程（04）" 八.2, Welford and
+// Chan et al.), then the CTA's states are merged in a fixed tree.  Pass 2:
+// every CTA of a row merges the row's S states in the same fixed tree (so all
+// of them normalise with identical statistics) and streams its piece again.
+struct Chan {
+    float n, mean, m2;
+};
+
+__device__ __forceinline__ Chan chan_merge(Chan a, Chan b) {
+    if (a.n == 0.f) return b;
+    if (b.n == 0.f) return a;
+    const float n = a.n + b.n, delta = b.mean - a.mean, fb = b.n / n;
+    return {n, fmaf(delta, fb, a.mean), a.m2 + b.m2 + delta * delta * a.n * fb};
+}
+
+// Merge the CTA's per-thread states; the result is valid in thread 0.
+template <int NW>
+__device__ __forceinline__ Chan block_chan_to_thread0(Chan c, float4 *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Chan o;
+        o.n = __shfl_down_sync(0xffffffffu, c.n, off);
+        o.mean = __shfl_down_sync(0xffffffffu, c.mean, off);
+        o.m2 = __shfl_down_sync(0xffffffffu, c.m2, off);
+        if (lane + off < 32) c = chan_merge(c, o);
+    }
+    if (lane == 0) red[warp] = make_float4(c.n, c.mean, c.m2, 0.f);
+    __syncthreads();
+    if (warp == 0) {
+        c = Chan{0.f, 0.f, 0.f};
+        if (lane < NW) {
+            const float4 q = red[lane];
+            c = Chan{q.x, q.y, q.z};
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            Chan o;
+            o.n = __shfl_down_sync(0xffffffffu, c.n, off);
+            o.mean = __shfl_down_sync(0xffffffffu, c.mean, off);
+            o.m2 = __shfl_down_sync(0xffffffffu, c.m2, off);
+            if (lane + off < 32) c = chan_merge(c, o);
+        }
+    }
+    return c;
+}
+
+template <Dt D, int G, int EPT, int U>
+__global__ void __launch_bounds__(G) layernorm_split_stats_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    const char *xrow = reinterpret_cast<const char *>(a.x) + q.row * a.N * Elem<D>::kBytes;
+    pdl_wait();
+    float p;
+    {
+        float t[1];
+        load_unit<D, 1, Hint::Keep>(xrow, 0, t);
+        p = t[0];
+    }
+    Chan st{0.f, 0.f, 0.f};
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U];
+        int cnt = 0;
+        float s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                load_unit<D, U, Hint::Keep>(xrow, ui * U, v[j]);
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    v[j][k] -= p;
+                    s1 += v[j][k];
+                }
+                cnt += U;
+            }
+        }
+        if (cnt == 0) continue;
+        const float tm = s1 / (float)cnt;
+        float s2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const float c = v[j][k] - tm;
+                    s2 = fmaf(c, c, s2);
+                }
+            }
+        }
+        st = chan_merge(st, Chan{(float)cnt, tm, s2});
+    }
+    __shared__ float4 red[32];
+    st = block_chan_to_thread0<G / 32>(st, red);
+    if (threadIdx.x == 0)
+        reinterpret_cast<float4 *>(a.ws)[q.row * a.cs + q.p] = make_float4(st.n, st.mean, st.m2, p);
+    pdl_trigger();
+}
+
+template <Dt D, int G, int EPT, int U>
+__global__ void __launch_bounds__(G) layernorm_split_apply_kernel(const RowArgs a) {
+    constexpr int NU = EPT / U;
+    const int64_t nunits = a.N / U;
+    const Piece q = make_piece(a, nunits);
+    const int64_t row_off = q.row * a.N * Elem<D>::kBytes;
+    const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    pdl_wait();
+    Chan st{0.f, 0.f, 0.f};
+    if (threadIdx.x < a.cs) {
+        const float4 w = reinterpret_cast<const float4 *>(a.ws)[q.row * a.cs + threadIdx.x];
+        st = Chan{w.x, w.y, w.z};
+    }
+    __shared__ float4 red[32];
+    __shared__ float2 stats;
+    st = block_chan_to_thread0<G / 32>(st, red);
+    if (threadIdx.x == 0) stats = make_float2(st.mean, rsqrtf(st.m2 / (float)a.N + a.eps));
+    const float p = reinterpret_cast<const float4 *>(a.ws)[q.row * a.cs].w;  // pass 1's pivot
+    __syncthreads();
+    const float mu = stats.x, r = stats.y;
+    char *yrow = reinterpret_cast<char *>(a.y) + row_off;
+    for (int64_t base = q.u0; base < q.u1; base += (int64_t)G * NU) {
+        float v[NU][U], g[NU][U], b[NU][U];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                load_unit<D, U>(xrow, ui * U, v[j]);
+                load_unit<D, U, Hint::ReadOnly>(a.gamma, ui * U, g[j]);
+                load_unit<D, U, Hint::ReadOnly>(a.beta, ui * U, b[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + threadIdx.x;
+            if (ui < q.u1) {
+                float o[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) o[k] = fmaf(((v[j][k] - p) - mu) * r, g[j][k], b[j][k]);
+                store_unit<D, U>(yrow, ui * U, o);
+            }
+        }
+    }
+    pdl_trigger();
+}
+
+}  // namespace osr
