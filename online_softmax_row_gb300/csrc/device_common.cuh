@@ -78,6 +78,64 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return q;
 }
 
+// ---------------------------------------------------------------- f32x2
+// Two binary32 lanes in one 64-bit register pair, for the packed arithmetic
+// of sm_100-family SMs (PTX add / sub / mul / fma .rn.f32x2).  Each lane is
+// rounded exactly as the scalar instruction rounds it, so a lane's result is
+// unchanged; one instruction does the work of two.
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// bfloat16 pair (element 2k in the low half) <-> binary32 pair
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) {
+    return f2_make(bf16_lo(w), bf16_hi(w));
+}
+__device__ __forceinline__ uint32_t bf16x2_from_f2(uint64_t v) {
+    return pack_bf16x2(f2_lo(v), f2_hi(v));
+}
+// pair k (elements 2k, 2k+1) of a 16-byte vector of dtype D: four bfloat16
+// pairs or two binary32 pairs
+template <Dt D>
+__device__ __forceinline__ uint64_t f2_of(const uint4 &q, int k) {
+    if constexpr (D == Dt::BF16)
+        return f2_from_bf16x2(k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w);
+    else
+        return k == 0 ? f2_make(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : f2_make(__uint_as_float(q.z), __uint_as_float(q.w));
+}
+
 // ---------------------------------------------------------------- loads
 // A "unit" is U consecutive elements: one 16-byte vector (U = kVec) or one
 // scalar (U = 1).  `e` is the element offset of the unit from `base`.

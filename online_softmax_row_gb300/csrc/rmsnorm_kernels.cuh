@@ -1,5 +1,5 @@
-// rmsnorm_kernels.cuh -- RMSNorm and fused residual-add + RMSNorm kernels: the register-cached
-// row/cluster kernel and the two split-row passes.
+// rmsnorm_kernels.cuh -- RMSNorm and fused residual-add + RMSNorm kernels: the
+// register-cached row/cluster kernel and the two split-row passes.
 #pragma once
 
 #include "row_common.cuh"

@@ -1,5 +1,5 @@
-// softmax_kernels.cuh -- softmax (and log-softmax) kernels: the register-cached row/cluster kernel
-// and the two split-row passes.
+// softmax_kernels.cuh -- softmax (and log-softmax) kernels: the register-cached
+// row/cluster kernel and the two split-row passes.
 #pragma once
 
 #include "row_common.cuh"
