@@ -61,6 +61,7 @@ def _configure(lib):
         lib.orc_softmax_chunked_stats.argtypes = [P, I, I64, I64, I64, P, P]
         lib.orc_log_softmax.argtypes = [P, I, I64, I64, P]
         lib.orc_logsumexp_argmax.argtypes = [P, I, I64, I64, P, P]
+        lib.orc_topk.argtypes = [P, I, I64, I64, I64, P, P, P, P]
         lib.orc_layernorm.argtypes = [P, P, P, I, D, I64, I64, P, P, P]
         lib.orc_welford.argtypes = [P, I, I64, I64, P, P, P]
         lib.orc_chan_merge.argtypes = [D, D, D, D, D, D, P, P, P]
@@ -236,6 +237,24 @@ def logsumexp_argmax(x: np.ndarray):
     am = np.empty(M, dtype=np.int64)
     _load().orc_logsumexp_argmax(_ptr(x), _dt(x), M, N, _ptr(lse), _ptr(am))
     return lse, am
+
+
+def topk(x: np.ndarray, k: int):
+    """Per row, the k largest values in the top-k order (value descending,
+    equal values by lower index, NaN above every number), their column
+    indices, the softmax of those k values and the row's log-sum-exp.
+    Returns (values float64 [M, k], indices int64 [M, k], probs float64
+    [M, k], lse float64 [M])."""
+    x = _c(x)
+    M, N = _rows(x)
+    if not 1 <= k <= N:
+        raise ValueError("need 1 <= k <= N")
+    vals = np.empty((M, k), dtype=np.float64)
+    idx = np.empty((M, k), dtype=np.int64)
+    probs = np.empty((M, k), dtype=np.float64)
+    lse = np.empty(M, dtype=np.float64)
+    _load().orc_topk(_ptr(x), _dt(x), M, N, int(k), _ptr(vals), _ptr(idx), _ptr(probs), _ptr(lse))
+    return vals, idx, probs, lse
 
 
 def layernorm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float,

@@ -18,6 +18,7 @@
  *   [AZ]  "GPU Kernel 工程（04）：共享内存与 reduction——softmax、LayerNorm
  *          与 online softmax" (arganzheng.life)
  *   [AR]  "Softmax 与归一化", CUDA 进阶手册 (anrans.github.io)
+ *   [LL]  "第23讲：为什么Attention必须先算Max？" (lilinji.mintlify.site)
  *
  * Storage types: 0 = binary32, 1 = bfloat16 (the upper 16 bits of a binary32).
  * Every function takes rows stored contiguously, row-major, row stride equal
@@ -25,6 +26,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -316,5 +318,55 @@ void orc_softmax_chunked_stats(const void *x, int dt, int64_t M, int64_t N,
         }
         m_out[i] = m;
         d_out[i] = d;
+    }
+}
+
+/* Top-k sampling prologue of a row, [AR] exercise 2 ("大词表采样": sampling
+ * needs no full softmax -- greedy needs the argmax, top-k picks the k largest
+ * logits first and takes the softmax of those):
+ *   order: element a precedes b when x_a > x_b, or x_a == x_b and a < b
+ *          (-0 and +0 are equal; a NaN ranks above every number);
+ *   values[t], indices[t]: the t-th element of the row in that order, t < k;
+ *   probs[t] = exp(values[t] - values[0]) / sum_{s<k} exp(values[s] - values[0]);
+ *   lse (optional) = log sum_j exp(x_j) of the whole row, m + log d with the
+ *   m and d of the three-pass softmax.
+ * The order is the plain definition: the whole row is sorted (qsort) and the
+ * first k taken. */
+struct topk_item {
+    double v;
+    int64_t i;
+};
+
+static int topk_cmp(const void *pa, const void *pb) {
+    const struct topk_item *a = (const struct topk_item *)pa, *b = (const struct topk_item *)pb;
+    const int an = isnan(a->v), bn = isnan(b->v);
+    if (an != bn) return an ? -1 : 1;
+    if (!an && a->v != b->v) return a->v > b->v ? -1 : 1;
+    return a->i < b->i ? -1 : (a->i > b->i ? 1 : 0);
+}
+
+void orc_topk(const void *x, int dt, int64_t M, int64_t N, int64_t k, double *values,
+              int64_t *indices, double *probs, double *lse) {
+#pragma omp parallel for schedule(dynamic) num_threads(g_threads)
+    for (int64_t i = 0; i < M; ++i) {
+        struct topk_item *it = (struct topk_item *)malloc((size_t)N * sizeof(struct topk_item));
+        for (int64_t j = 0; j < N; ++j) {
+            it[j].v = elem(x, dt, i * N + j);
+            it[j].i = j;
+        }
+        qsort(it, (size_t)N, sizeof(struct topk_item), topk_cmp);
+        double z = 0.0;
+        for (int64_t t = 0; t < k; ++t) z += exp(it[t].v - it[0].v);
+        for (int64_t t = 0; t < k; ++t) {
+            values[i * k + t] = it[t].v;
+            indices[i * k + t] = it[t].i;
+            if (probs) probs[i * k + t] = exp(it[t].v - it[0].v) / z;
+        }
+        free(it);
+        if (lse) {
+            double m, d;
+            row_max_sum(x, dt, i, N, &m, &d, 0);
+            lse[i] = m + log(d);
+        }
     }
 }

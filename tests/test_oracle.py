@@ -530,3 +530,73 @@ def test_welford_and_chan_merge_equal_two_pass():
         nn, mm, qq = st[0]
         assert nn == 777 and abs(mm - mu[0]) <= 1e-13 * mu[0]
         assert abs(qq / nn - var[0]) <= 1e-9 * var[0]
+
+
+# --------------------------------------------------------------- top-k prologue
+
+def test_golden_topk_full_row_is_the_softmax_of_2_4_1_sorted():
+    # with k = N the top-k softmax is the row's softmax, listed largest first
+    g = load_golden("softmax_2_4_1.txt")
+    x = f32(nums(g["x"]))[None, :]
+    vals, idx, probs, lse = oracle.topk(x, 3)
+    assert idx.tolist() == [[1, 0, 2]]
+    assert vals.tolist() == [[4.0, 2.0, 1.0]]
+    y = nums(g["expect.y"])
+    np.testing.assert_allclose(probs[0], [y[1], y[0], y[2]], atol=float(g["tol"]))
+    np.testing.assert_allclose(lse[0], 4.0 + math.log(float(g["expect.d"])), atol=1e-4)
+
+
+def lexsort_topk(x: np.ndarray, k: int):
+    """Library order: numpy's stable lexsort on (value descending, index)."""
+    order = np.lexsort((np.arange(x.shape[1])[None, :].repeat(x.shape[0], 0), -x), axis=1)
+    return order[:, :k]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,k", [(3, 17, 5), (4, 1000, 50), (2, 4096, 1024), (5, 64, 64)])
+def test_topk_matches_numpy_lexsort(M, N, k, dt):
+    g = torch.Generator().manual_seed(M * 7919 + N + k)
+    x = torch.randn(M, N, generator=g) * 4
+    x[:, ::7] = torch.round(x[:, ::7])  # plenty of equal values
+    if dt == "bf16":
+        xb = x.to(torch.bfloat16)       # bf16 rounding adds more ties
+        arr, xs = bf16_bits(xb), xb.float().numpy().astype(np.float64)
+    else:
+        arr, xs = x.numpy(), x.numpy().astype(np.float64)
+    vals, idx, probs, lse = oracle.topk(arr, k)
+    want = lexsort_topk(xs, k)
+    assert np.array_equal(idx, want)
+    assert np.array_equal(vals, np.take_along_axis(xs, want, axis=1))
+
+
+def test_topk_matches_torch_topk_on_distinct_values():
+    g = torch.Generator().manual_seed(5)
+    x = torch.randperm(5000, generator=g).reshape(5, 1000).float() * 0.25 - 300
+    vals, idx, _, _ = oracle.topk(x.numpy(), 37)
+    tv, ti = torch.topk(x.double(), 37, dim=1, sorted=True)
+    assert np.array_equal(idx, ti.numpy())
+    assert np.array_equal(vals, tv.numpy())
+
+
+def test_topk_ties_nan_and_signed_zero():
+    x = f32([[1.0, 3.0, 3.0, -0.0, 0.0, np.nan, 3.0, -np.inf]])
+    vals, idx, _, _ = oracle.topk(x, 8)
+    assert idx.tolist() == [[5, 1, 2, 6, 0, 3, 4, 7]]  # NaN first, equal values by index
+    assert math.isnan(vals[0, 0]) and vals[0, 1:].tolist()[:4] == [3.0, 3.0, 3.0, 1.0]
+    # k = 1 is the argmax (first index of the maximum) of a NaN-free row
+    y = f32([[0.5, 2.0, -1.0, 2.0, 2.0]])
+    assert oracle.topk(y, 1)[1].tolist() == [[1]]
+    assert oracle.logsumexp_argmax(y)[1].tolist() == [1]
+
+
+@pytest.mark.parametrize("k", [1, 7, 200])
+def test_topk_probs_and_lse_match_torch_fp64(k):
+    g = torch.Generator().manual_seed(k)
+    x = torch.randn(6, 777, generator=g) * 5
+    x[2, 100:] = -math.inf  # a masked row: the mass sits on the first 100
+    vals, idx, probs, lse = oracle.topk(x.numpy(), k)
+    np.testing.assert_allclose(probs, torch.softmax(torch.from_numpy(vals), -1).numpy(),
+                               rtol=1e-14, atol=1e-300)
+    np.testing.assert_allclose(probs.sum(axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(lse, torch.logsumexp(x.double(), -1).numpy(), rtol=1e-15)
+    assert np.all(vals[:, 1:] <= vals[:, :-1])

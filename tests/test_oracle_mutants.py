@@ -71,6 +71,21 @@ MUTANTS = [
     ("chan merge drops the between-group term",
      "*m2 = qa + qb + delta * delta * na * nb / nn;",
      "*m2 = qa + qb;"),
+    ("top-k ties take the higher index first",
+     "return a->i < b->i ? -1 : (a->i > b->i ? 1 : 0);",
+     "return a->i > b->i ? -1 : (a->i < b->i ? 1 : 0);"),
+    ("top-k sorted ascending",
+     "if (!an && a->v != b->v) return a->v > b->v ? -1 : 1;",
+     "if (!an && a->v != b->v) return a->v < b->v ? -1 : 1;"),
+    ("top-k ranks NaN last",
+     "if (an != bn) return an ? -1 : 1;",
+     "if (an != bn) return an ? 1 : -1;"),
+    ("top-k softmax normalised without the first value",
+     "for (int64_t t = 0; t < k; ++t) z += exp(it[t].v - it[0].v);",
+     "for (int64_t t = 1; t < k; ++t) z += exp(it[t].v - it[0].v);"),
+    ("top-k softmax not shifted by the largest value",
+     "if (probs) probs[i * k + t] = exp(it[t].v - it[0].v) / z;",
+     "if (probs) probs[i * k + t] = exp(it[t].v) / z;"),
     ("chunk summary sums exp without its max",
      "for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - cm);",
      "for (int64_t j = c0; j < c1; ++j) cd += exp(elem(x, dt, i * N + j) - m);"),
@@ -85,6 +100,8 @@ PARAMS = {
     "test_logsumexp_constant_row_closed_form": [(7,)],
     "test_log_softmax_and_logsumexp_match_torch_fp64": [((3, 17),)],
     "test_layernorm_matches_torch_fp64": [((3, 33), "f32")],
+    "test_topk_matches_numpy_lexsort": [(3, 17, 5, "f32"), (4, 1000, 50, "bf16")],
+    "test_topk_probs_and_lse_match_torch_fp64": [(7,)],
 }
 
 
