@@ -52,7 +52,7 @@ NOMINAL_HBM_GBS = 8000.0          # NVIDIA's public per-GPU HBM3e figure for GB3
 FALLBACK_HBM_GBS = 6800.0         # used only when no measured peak file exists
 DEFAULT_WORKLOAD = "fused_add_rmsnorm_bf16_8192x4096"
 OP_CODE = {"rmsnorm": 0, "fused_add_rmsnorm": 1, "softmax": 2, "log_softmax": 3, "logsumexp": 4,
-           "layernorm": 5}
+           "layernorm": 5, "topk": 6}
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -97,6 +97,8 @@ def kernel_units(w) -> list[str]:
         return [f"k_softmax_{d[w.in_dtype]}{d[w.out_dtype]}.cu", "k_staged.cu"]
     if w.op == "logsumexp":
         return ["k_lse.cu"]
+    if w.op == "topk":
+        return ["k_topk.cu"]
     prefix = {"rmsnorm": "k_rms", "fused_add_rmsnorm": "k_fused", "layernorm": "k_ln"}[w.op]
     return [f"{prefix}_{d[w.in_dtype]}.cu"]
 
@@ -204,6 +206,11 @@ def add_outputs(w, s, device):
     elif w.op == "logsumexp":
         s["y"] = torch.empty(w.M, dtype=torch.float32, device=device)
         s["arg"] = torch.empty(w.M, dtype=torch.int64, device=device)
+    elif w.op == "topk":
+        s["y"] = torch.empty(w.M, w.k, dtype=torch.float32, device=device)
+        s["arg"] = torch.empty(w.M, w.k, dtype=torch.int64, device=device)
+        s["probs"] = torch.empty(w.M, w.k, dtype=torch.float32, device=device)
+        s["lse"] = torch.empty(w.M, dtype=torch.float32, device=device)
     else:
         s["y"] = torch.empty_like(s["x"])
     return s
@@ -244,6 +251,15 @@ def call(osr, w, s):
                                    torch.cuda.current_stream(x.device).cuda_stream)
         if st != 0:
             raise RuntimeError(f"osr_row_logsumexp: status {st}")
+        return s["y"]
+    if w.op == "topk":
+        lib = osr.library()
+        x = s["x"]
+        st = lib.osr_row_topk(x.data_ptr(), s["y"].data_ptr(), s["arg"].data_ptr(), s["probs"].data_ptr(),
+                              s["lse"].data_ptr(), w.M, w.N, w.k, 1 if x.dtype == torch.bfloat16 else 0,
+                              torch.cuda.current_stream(x.device).cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"osr_row_topk: status {st}")
         return s["y"]
     if w.op == "rmsnorm":
         return osr.rmsnorm_fwd(s["x"], s["gamma"], w.eps, out=s["y"])
@@ -341,7 +357,7 @@ def time_e2e(osr, w, steps, warmup, device):
     host_in = {k: v.pin_memory() for k, v in inp.items()}
     dev = add_outputs(w, {k: torch.empty_like(v, device=device) for k, v in inp.items()}, device)
     outs = ["y"] + (["residual"] if w.op == "fused_add_rmsnorm" else []) + \
-        (["arg"] if w.op == "logsumexp" else [])
+        (["arg"] if w.op in ("logsumexp", "topk") else []) + (["probs", "lse"] if w.op == "topk" else [])
     host_out = {k: torch.empty(dev[k].shape, dtype=dev[k].dtype, pin_memory=True) for k in outs}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in outs)
@@ -414,7 +430,7 @@ def cpu_baseline_for(w, budget_s=8.0):
 
 def _oracle_inputs(w, rows):
     """Oracle-format inputs (float32, or uint16 bf16 bits) for the first rows."""
-    if w.op in ("softmax", "log_softmax", "logsumexp"):
+    if w.op in ("softmax", "log_softmax", "logsumexp", "topk"):
         inp = workloads.softmax_inputs(rows, w.N, w.in_dtype, w.sigma, 0, w.shift, w.spikes_per_row,
                                        w.spike, seed=0, mask=w.mask)
     elif w.op == "layernorm":
@@ -436,6 +452,8 @@ def _run_oracle(oracle, w, inp):
         return oracle.round_to(oracle.log_softmax(inp["x"]), w.out_dtype)
     if w.op == "logsumexp":
         return oracle.logsumexp_argmax(inp["x"])
+    if w.op == "topk":
+        return oracle.topk(inp["x"], w.k)
     if w.op == "rmsnorm":
         y = oracle.rmsnorm(inp["x"], inp["gamma"], w.eps)
         return oracle.round_to(y, w.out_dtype)

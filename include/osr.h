@@ -175,6 +175,32 @@ osr_status osr_log_softmax_rows(const void *x, void *y, int64_t M, int64_t N, os
 osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t M, int64_t N,
                              osr_dtype in_dt, void *stream);
 
+/*
+ * Top-k sampling prologue of each row, from one read of the row
+ * ("Softmax 与归一化" (anrans.github.io), exercise 2 "大词表采样": top-k
+ * sampling takes the k largest logits first and the softmax of only those):
+ *   values  [M][k] binary32: the k largest x[i, :], largest first; equal
+ *                            values in increasing column order; a NaN ranks
+ *                            above every number, -0 and +0 are equal
+ *   indices [M][k] int64:    their column indices
+ *   probs   [M][k] binary32: exp(values[t] - values[0]) / sum_s exp(values[s] -
+ *                            values[0]) over the k, may be NULL
+ *   lse     [M] binary32:    log(sum_j exp(x[i, j])) of the whole row, as
+ *                            osr_row_logsumexp, may be NULL
+ * x: [M][N] row-major, dtype in_dt (any of osr_dtype), any alignment (16-byte
+ * aligned rows with N a multiple of 16 bytes take the vector loads).  Values
+ * are the row's own values converted exactly to binary32; the selection is
+ * exact (no rounding decides it), so values and indices are unique.
+ * Limits: 1 <= k <= min(N, 1024) (k > N: OSR_ERR_INVALID, k > 1024:
+ * OSR_ERR_UNSUPPORTED); a row must fit 16 CTAs' shared memory (192 KiB of
+ * elements each: N <= 1.5 Mi bfloat16 or 786 Ki binary32) and N < 2^31,
+ * else OSR_ERR_UNSUPPORTED.  Outputs must not overlap x or each other
+ * (OSR_ERR_ALIAS).  All buffers are caller-owned device memory; the call is
+ * asynchronous on `stream` and allocates nothing.
+ */
+osr_status osr_row_topk(const void *x, float *values, int64_t *indices, float *probs, float *lse,
+                        int64_t M, int64_t N, int64_t k, osr_dtype in_dt, void *stream);
+
 /* Static description of a status code (never NULL). */
 const char *osr_status_string(osr_status s);
 
@@ -185,7 +211,8 @@ int osr_last_cuda_error(void);
 /*
  * Which kernel the length-based dispatcher picks, without touching a GPU.
  *   op        0 = RMSNorm, 1 = fused residual-add + RMSNorm, 2 = softmax,
- *             3 = log-softmax, 4 = log-sum-exp / argmax, 5 = LayerNorm
+ *             3 = log-softmax, 4 = log-sum-exp / argmax, 5 = LayerNorm,
+ *             6 = top-k (the geometry for k = 64; k sizes only the sort)
  *   vec_ok    1 if every buffer is 16-byte aligned (the 128-bit path)
  *   sm_count  streaming multiprocessors of the target device (152 on GB300)
  *   buf       receives a NUL-terminated description, e.g.

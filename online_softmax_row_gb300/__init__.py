@@ -16,6 +16,7 @@ softmax_rows         osr_softmax_rows
 softmax_rows_stats   osr_softmax_rows_stats
 log_softmax_rows     osr_log_softmax_rows
 row_logsumexp        osr_row_logsumexp
+row_topk             osr_row_topk
 plan_describe        osr_plan_describe
 bench_copy           osr_bench_copy
 device_fault         osr_device_fault
@@ -31,12 +32,13 @@ import torch
 from . import build as _build
 
 __all__ = ["OsrError", "rmsnorm_fwd", "layernorm_fwd", "OP_LAYERNORM", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
-           "log_softmax_rows", "row_logsumexp", "OP_LOG_SOFTMAX", "OP_LOGSUMEXP",
+           "log_softmax_rows", "row_logsumexp", "row_topk", "OP_LOG_SOFTMAX", "OP_LOGSUMEXP",
+           "OP_TOPK",
            "plan_describe", "bench_copy", "device_fault", "library", "library_path", "OP_RMSNORM",
            "OP_FUSED",
            "OP_SOFTMAX"]
 
-OP_RMSNORM, OP_FUSED, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_LOGSUMEXP, OP_LAYERNORM = 0, 1, 2, 3, 4, 5
+OP_RMSNORM, OP_FUSED, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_LOGSUMEXP, OP_LAYERNORM, OP_TOPK = 0, 1, 2, 3, 4, 5, 6
 _DT = {torch.float32: 0, torch.bfloat16: 1}
 _DT_NAME = {"f32": 0, "bf16": 1}
 _STATUS = {0: "OSR_OK", 1: "OSR_ERR_INVALID", 2: "OSR_ERR_ALIGN", 3: "OSR_ERR_ALIAS",
@@ -83,9 +85,10 @@ def library():
         lib.osr_log_softmax_rows.argtypes = [P, P, I64, I64, I, I, P]
         lib.osr_layernorm_fwd.argtypes = [P, P, P, F, P, I64, I64, I, P]
         lib.osr_row_logsumexp.argtypes = [P, P, P, I64, I64, I, P]
+        lib.osr_row_topk.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
         for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
                    "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy",
-                   "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp",
+                   "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp", "osr_row_topk",
                    "osr_layernorm_fwd"):
             getattr(lib, fn).restype = I
         _lib = lib
@@ -249,6 +252,26 @@ def row_logsumexp(x: torch.Tensor, want_lse: bool = True, want_argmax: bool = Tr
     _check(_run(x, lib.osr_row_logsumexp, x.data_ptr(), lse.data_ptr() if lse is not None else None,
                 am.data_ptr() if am is not None else None, M, N, _DT[x.dtype]), "osr_row_logsumexp")
     return lse, am
+
+
+def row_topk(x: torch.Tensor, k: int, want_probs: bool = True, want_lse: bool = True):
+    """Per row: the k largest values (float32, largest first, equal values by
+    column), their column indices (int64), the softmax of those k values
+    (float32) and the row's log-sum-exp (float32), reading x once.  Returns
+    (values, indices, probs or None, lse or None); leading dimensions of x
+    are kept."""
+    M, N = _rows(x, "x")
+    lead = x.shape[:-1]
+    values = torch.empty(*lead, k, dtype=torch.float32, device=x.device)
+    indices = torch.empty(*lead, k, dtype=torch.int64, device=x.device)
+    probs = torch.empty(*lead, k, dtype=torch.float32, device=x.device) if want_probs else None
+    lse = torch.empty(lead, dtype=torch.float32, device=x.device) if want_lse else None
+    lib = _lib or library()
+    _check(_run(x, lib.osr_row_topk, x.data_ptr(), values.data_ptr(), indices.data_ptr(),
+                probs.data_ptr() if probs is not None else None,
+                lse.data_ptr() if lse is not None else None, M, N, int(k), _DT[x.dtype]),
+           "osr_row_topk")
+    return values, indices, probs, lse
 
 
 def plan_describe(op: int, M: int, N: int, in_dtype: str = "f32", out_dtype: str | None = None,

@@ -20,6 +20,7 @@
 
 #include "../../include/osr.h"
 #include "launch.h"
+#include "topk.h"
 
 namespace osr {
 namespace {
@@ -390,6 +391,59 @@ osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_
     return OSR_OK;
 }
 
+// Top-k geometry: one cluster of cs CTAs per row, each caching a piece of
+// the row (at most kTopkMaxPieceBytes) in shared memory.  The fewest CTAs
+// that hold the row, raised so that few rows still spread over the SMs
+// (powers of two up to 8, or up to 16 when even 16 per row leave SMs idle),
+// but never so far that a CTA gets less than one vector per thread.
+// OSR_FORCE_KERNEL="topk:cs=<n>" picks cs (tests).
+struct TopkPlan {
+    int cs = 1;
+    int64_t chunk = 0;
+    int sort_n = 1;
+    uint32_t region0 = 0;
+    size_t smem = 0;
+    bool forced = false;
+};
+
+constexpr size_t kTopkSmemLimit = 227 * 1024 - 256;  // dynamic shared memory per CTA
+
+osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, int sms,
+                     int max_cluster, TopkPlan *tp) {
+    *tp = TopkPlan();
+    const int eb = elem_bytes(dt);
+    const int u = vec ? vec_elems(dt) : 1;
+    const int64_t cs_min = cdiv(N * eb, kTopkMaxPieceBytes);
+    int64_t cs = cs_min;
+    const char *force = getenv("OSR_FORCE_KERNEL");
+    int64_t fcs = 0;
+    if (force && strncmp(force, "topk", 4) == 0) {
+        if (!parse_kv(force, "cs", &fcs) || fcs < 1) return OSR_ERR_UNSUPPORTED;
+        cs = fcs;
+        tp->forced = true;
+    } else {
+        int64_t fill = pow2_at_least(cdiv(2 * (int64_t)sms, M > 0 ? M : 1));
+        const int64_t cap = M * 16 <= sms ? 16 : 8;
+        if (fill > cap) fill = cap;
+        if (fill > cs) cs = fill;
+        while (cs > cs_min && cdiv(N, cs) < (int64_t)kTopkThreads * u) cs = cs / 2 > cs_min ? cs / 2 : cs_min;
+    }
+    if (cs > max_cluster || cs > kTopkMaxCluster) return OSR_ERR_UNSUPPORTED;
+    const int64_t chunk = cdiv(cdiv(N, cs), u) * u;
+    if (chunk * eb > kTopkMaxPieceBytes) return OSR_ERR_UNSUPPORTED;
+    const int64_t sort_n = pow2_at_least(k);
+    int64_t r0 = chunk * eb > sort_n * 8 ? chunk * eb : sort_n * 8;
+    r0 = cdiv(r0, 16) * 16;
+    const size_t smem = topk_smem_bytes((uint32_t)r0, k);
+    if (smem > kTopkSmemLimit) return OSR_ERR_UNSUPPORTED;
+    tp->cs = (int)cs;
+    tp->chunk = chunk;
+    tp->sort_n = (int)sort_n;
+    tp->region0 = (uint32_t)r0;
+    tp->smem = smem;
+    return OSR_OK;
+}
+
 osr_status execute(Op op, osr_dtype in_dt, osr_dtype out_dt, RowArgs a, const Plan &p,
                    cudaStream_t st) {
     const int64_t M = a.M;
@@ -509,10 +563,19 @@ int osr_version(void) { return 100; }
 
 osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                              int vec_ok, int sm_count, char *buf, size_t buf_len) {
-    if (op < 0 || op > 5 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
+    if (op < 0 || op > 6 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || !buf || buf_len == 0 ||
         sm_count <= 0)
         return OSR_ERR_INVALID;
     if ((op < 2 || op == 5) && in_dt != out_dt) return OSR_ERR_UNSUPPORTED;
+    if (op == 6) {  // top-k: the plan for k = 64 (k changes only the sort buffer)
+        const bool tvec = vec_ok && (N % vec_elems(in_dt)) == 0;
+        TopkPlan tp;
+        const osr_status ts = topk_plan(M, N, N < 64 ? N : 64, in_dt, tvec, sm_count, 16, &tp);
+        if (ts != OSR_OK) return ts;
+        snprintf(buf, buf_len, "topk cs=%d piece=%lldB %s", tp.cs,
+                 (long long)(tp.chunk * elem_bytes(in_dt)), tvec ? "vec" : "scalar");
+        return OSR_OK;
+    }
     osr_status s = check_sizes(M, N);
     if (s != OSR_OK) return s;
     const bool vec = vec_ok && (N % vec_elems(in_dt)) == 0;
@@ -705,6 +768,59 @@ osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t
     const cudaError_t e = in_dt == OSR_F32
         ? launch_lse<Dt::F32>(a, lp.g, lp.cs > 1, vec, lp.grid, (cudaStream_t)stream)
         : launch_lse<Dt::BF16>(a, lp.g, lp.cs > 1, vec, lp.grid, (cudaStream_t)stream);
+    return e == cudaSuccess ? OSR_OK : cuda_fail(e);
+}
+
+osr_status osr_row_topk(const void *x, float *values, int64_t *indices, float *probs, float *lse,
+                        int64_t M, int64_t N, int64_t k, osr_dtype in_dt, void *stream) {
+    osr_status s = check_sizes(M, N);
+    if (s != OSR_OK) return s;
+    if (!dtype_ok(in_dt) || k < 1 || k > N) return OSR_ERR_INVALID;
+    if (k > kTopkMaxK || N >= ((int64_t)1 << 31)) return OSR_ERR_UNSUPPORTED;
+    if (M == 0) return OSR_OK;
+    if (!x || !values || !indices) return OSR_ERR_INVALID;
+    const int64_t xb = M * N * elem_bytes(in_dt), vb = M * k * 4, ib = M * k * 8, lb = M * 4;
+    const void *bufs[4] = {values, indices, probs, lse};
+    const int64_t lens[4] = {vb, ib, vb, lb};
+    for (int i = 0; i < 4; ++i) {
+        if (!bufs[i]) continue;
+        if (overlaps(bufs[i], lens[i], x, xb)) return OSR_ERR_ALIAS;
+        for (int j = i + 1; j < 4; ++j)
+            if (bufs[j] && overlaps(bufs[i], lens[i], bufs[j], lens[j])) return OSR_ERR_ALIAS;
+    }
+    for (int i = 0; i < 4; ++i)
+        if (bufs[i] && !device_accessible(bufs[i])) return OSR_ERR_INVALID;
+    if (!device_accessible(x)) return OSR_ERR_INVALID;
+    DeviceInfo di;
+    if ((s = device_info(&di)) != OSR_OK) return s;
+    const bool vec = aligned16(x) && N % vec_elems(in_dt) == 0;
+    TopkPlan tp;
+    if ((s = topk_plan(M, N, k, in_dt, vec, di.sms, di.max_cluster, &tp)) != OSR_OK) return s;
+    if (M * tp.cs > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
+    // the cluster shape must be schedulable with this much shared memory
+    int n = 0;
+    cudaError_t e = in_dt == OSR_F32 ? topk_occupancy<Dt::F32>(vec, tp.cs, tp.smem, &n)
+                                     : topk_occupancy<Dt::BF16>(vec, tp.cs, tp.smem, &n);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return OSR_ERR_UNSUPPORTED;
+    }
+    if (n < 1) return OSR_ERR_UNSUPPORTED;
+    TopkArgs a = {};
+    a.x = x;
+    a.values = values;
+    a.indices = indices;
+    a.probs = probs;
+    a.lse = lse;
+    a.M = M;
+    a.N = N;
+    a.k = k;
+    a.chunk = tp.chunk;
+    a.cs = tp.cs;
+    a.sort_n = tp.sort_n;
+    a.region0 = tp.region0;
+    e = in_dt == OSR_F32 ? launch_topk<Dt::F32>(a, vec, tp.smem, (cudaStream_t)stream)
+                         : launch_topk<Dt::BF16>(a, vec, tp.smem, (cudaStream_t)stream);
     return e == cudaSuccess ? OSR_OK : cuda_fail(e);
 }
 

@@ -1,0 +1,43 @@
+// topk.h -- arguments, limits and launcher of the top-k sampling prologue
+// (k_topk.cu), declared apart from launch.h so the row kernels do not depend
+// on it.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+
+namespace osr {
+
+struct TopkArgs {
+    const void *x;     // [M][N] input rows
+    float *values;     // [M][k] the k largest values, largest first
+    int64_t *indices;  // [M][k] their column indices
+    float *probs;      // [M][k] softmax of the k values, may be null
+    float *lse;        // [M] log-sum-exp of the whole row, may be null
+    int64_t M, N, k;
+    int64_t chunk;     // elements per cluster CTA (a multiple of the vector width)
+    int cs;            // CTAs per row (cluster size)
+    int sort_n;        // power of two >= k: the sorting network's width
+    uint32_t region0;  // bytes of the piece / sort region at the start of shared memory
+};
+
+constexpr int kTopkThreads = 256;
+constexpr int64_t kTopkMaxK = 1024;
+constexpr int64_t kTopkMaxPieceBytes = 192 << 10;  // largest piece a CTA caches
+constexpr int kTopkMaxCluster = 16;
+
+// Dynamic shared memory of one CTA: piece (or sort buffer), per-warp
+// histograms, the published histogram (two buffers), the candidate list.
+inline size_t topk_smem_bytes(uint32_t region0, int64_t k) {
+    return (size_t)region0 + (size_t)(kTopkThreads / 32) * 256 * 4 + 2 * 256 * 4 + (size_t)k * 8;
+}
+
+template <Dt DI>
+cudaError_t launch_topk(const TopkArgs &a, bool vec, size_t smem, cudaStream_t st);
+template <Dt DI>
+cudaError_t topk_occupancy(bool vec, int cs, size_t smem, int *n);
+
+}  // namespace osr

@@ -207,3 +207,29 @@ def test_layernorm_plans_and_validation(lib):
     assert lib.osr_layernorm_fwd(P, P * 8, P * 16 + 8, f, P * 16, 4, 16, F32, None) == 3  # y over beta
     assert lib.osr_layernorm_fwd(P, P * 8, P * 12, f, P + 4, 4, 16, F32, None) == 3      # y over x
     assert lib.osr_layernorm_fwd(None, None, None, f, None, 0, 16, F32, None) == 0
+
+
+def test_topk_plans_and_validation(lib, monkeypatch):
+    D = osr.plan_describe
+    assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=8 piece=38016B vec"
+    assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=16 piece=19008B vec"   # one row: 16 CTAs
+    assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=8 piece=76032B vec"
+    assert D(osr.OP_TOPK, 8, 1000, "bf16") == "topk cs=1 piece=2000B vec"       # short rows: one CTA
+    assert D(osr.OP_TOPK, 3, 33, "bf16", vec_ok=False) == "topk cs=1 piece=66B scalar"
+    assert D(osr.OP_TOPK, 1, 786432, "f32") == "topk cs=16 piece=196608B vec"   # largest row
+    with pytest.raises(osr.OsrError):
+        D(osr.OP_TOPK, 1, 786433, "f32")                                        # beyond 16 x 192 KiB
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "topk:cs=4")
+    assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
+    monkeypatch.delenv("OSR_FORCE_KERNEL")
+    T = lib.osr_row_topk
+    assert T(P, P * 8, P * 16, None, None, 0, 16, 4, F32, None) == 0            # M == 0
+    assert T(P, P * 8, P * 16, None, None, 4, 16, 0, F32, None) == 1            # k < 1
+    assert T(P, P * 8, P * 16, None, None, 4, 16, 17, F32, None) == 1           # k > N
+    assert T(P, P * 8, P * 16, None, None, 4, 4096, 1025, F32, None) == 4       # k > 1024
+    assert T(P, None, P * 16, None, None, 4, 16, 4, F32, None) == 1             # NULL values
+    assert T(P, P * 8, None, None, None, 4, 16, 4, F32, None) == 1              # NULL indices
+    assert T(P, P + 8, P * 16, None, None, 4, 16, 4, F32, None) == 3            # values over x
+    assert T(P, P * 8, P * 8 + 8, None, None, 4, 16, 4, F32, None) == 3         # indices over values
+    assert T(P, P * 8, P * 16, P * 16 + 8, None, 4, 16, 4, F32, None) == 3      # probs over indices
+    assert T(P, P * 8, P * 16, P * 24, P * 24, 4, 16, 4, F32, None) == 3        # lse over probs

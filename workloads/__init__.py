@@ -26,7 +26,7 @@ ELEM_BYTES = {"f32": 4, "bf16": 2}
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "layernorm" | "softmax" | "log_softmax" | "logsumexp"
+    op: str                 # "rmsnorm" | "fused_add_rmsnorm" | "layernorm" | "softmax" | "log_softmax" | "logsumexp" | "topk"
     M: int
     N: int                  # row length (H for the norms)
     in_dtype: str
@@ -40,6 +40,7 @@ class Workload:
     spikes_per_row: int = 0
     spike: float = 30.0
     mask: str = ""          # "" | "causal" (square per head: query = row % N) | "keep:K"
+    k: int = 0              # top-k: entries selected per row
     l2_resident: bool = False
     note: str = ""
     extra: dict = field(default_factory=dict)
@@ -58,6 +59,8 @@ class Workload:
             return 2 * n * e_in + 2 * n * e_out + self.N * e_in
         if self.op == "logsumexp":  # reads the rows, writes a float and an int64 per row
             return n * e_in + self.M * (4 + 8)
+        if self.op == "topk":  # reads the rows; per row k values, indices and probs, one lse
+            return n * e_in + self.M * self.k * (4 + 8 + 4) + self.M * 4
         return n * e_in + n * e_out
 
 
@@ -94,6 +97,11 @@ WORKLOADS["logsumexp_argmax_vocab_bf16_64x152064"] = Workload(
     "logsumexp_argmax_vocab_bf16_64x152064", "logsumexp", 64, 152064, "bf16", "f32", sigma=4.0,
     spikes_per_row=8, l2_resident=True,
     note="sampling statistics of the vocabulary-logit rows: log-sum-exp and argmax, no probabilities")
+WORKLOADS["topk_vocab_bf16_64x152064_k50"] = Workload(
+    "topk_vocab_bf16_64x152064_k50", "topk", 64, 152064, "bf16", "f32", sigma=4.0,
+    spikes_per_row=8, l2_resident=True, k=50,
+    note="top-k sampling prologue of the vocabulary-logit rows: the 50 largest logits, "
+         "their indices, their softmax and the row log-sum-exp")
 WORKLOADS["softmax_causal_f32_57344x2048"] = Workload(
     "softmax_causal_f32_57344x2048", "softmax", 28 * 2048, 2048, "f32", "f32", sigma=3.0,
     mask="causal",
