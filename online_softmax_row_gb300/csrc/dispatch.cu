@@ -432,7 +432,9 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
     const int64_t chunk = cdiv(cdiv(N, cs), u) * u;
     if (chunk * eb > kTopkMaxPieceBytes) return OSR_ERR_UNSUPPORTED;
     const int64_t sort_n = pow2_at_least(k);
+    // the region holds the piece, and later the gathered lists or the sort
     int64_t r0 = chunk * eb > sort_n * 8 ? chunk * eb : sort_n * 8;
+    if (r0 < kTopkMinWords * 8) r0 = kTopkMinWords * 8;
     r0 = cdiv(r0, 16) * 16;
     const size_t smem = topk_smem_bytes((uint32_t)r0, k);
     if (smem > kTopkSmemLimit) return OSR_ERR_UNSUPPORTED;

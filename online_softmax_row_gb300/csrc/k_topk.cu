@@ -60,20 +60,48 @@ __device__ __forceinline__ float raw_to_f32(uint32_t bits, Dt dt) {
     return __uint_as_float(dt == Dt::BF16 ? bits << 16 : bits);
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Remote shared-memory loads.  volatile keeps them after the cluster
+// barrier (itself volatile, with a memory clobber); they have no clobber of
+// their own, so several can be in flight at once.
 __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
     uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ uint64_t ld_dsmem_u64(uint32_t addr) {
     uint64_t v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr));
     return v;
+}
+
+// dst[0, cnt) <- cnt words of another CTA's shared memory at `src`, four
+// remote loads in flight per thread
+__device__ __forceinline__ void copy_words(uint64_t *dst, uint32_t src, uint32_t cnt) {
+    for (uint32_t i0 = threadIdx.x; i0 < cnt; i0 += 4 * kTopkThreads) {
+        uint64_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t i = i0 + j * kTopkThreads;
+            v[j] = i < cnt ? ld_dsmem_u64(src + i * 8) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t i = i0 + j * kTopkThreads;
+            if (i < cnt) dst[i] = v[j];
+        }
+    }
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -119,44 +147,6 @@ __device__ __forceinline__ float block_sum_f(float v, float *scratch) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *scratch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = __reduce_max_sync(0xffffffffu, v);
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    uint32_t r = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) r = scratch[w] > r ? scratch[w] : r;
-    __syncthreads();
-    return r;
-}
-
-// Keys of the elements of a 16-byte vector of raw values (8 bfloat16 or 4
-// binary32), packed the same way.
-template <Dt DI>
-__device__ __forceinline__ uint4 keys_of(const uint4 &q) {
-    if constexpr (DI == Dt::BF16) {
-        auto k2 = [](uint32_t w) {
-            return topk_key(w & 0xffffu, Dt::BF16) | (topk_key(w >> 16, Dt::BF16) << 16);
-        };
-        return make_uint4(k2(q.x), k2(q.y), k2(q.z), k2(q.w));
-    } else {
-        return make_uint4(topk_key(q.x, DI), topk_key(q.y, DI), topk_key(q.z, DI),
-                          topk_key(q.w, DI));
-    }
-}
-
-// Key e of a 16-byte vector of keys.
-template <Dt DI>
-__device__ __forceinline__ uint32_t key_at(const uint4 &q, int e) {
-    if constexpr (DI == Dt::BF16) {
-        const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
-        return (e & 1) ? w >> 16 : w & 0xffffu;
-    } else {
-        return e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
-    }
-}
-
 // The number a key stands for (-0 comes back as +0, NaN as the quiet NaN).
 template <Dt DI>
 __device__ __forceinline__ float key_value(uint32_t key) {
@@ -168,254 +158,439 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     }
 }
 
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;  // per half: the larger number (a NaN loses to a number)
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Float value of element e of a 16-byte vector of raw values.
+template <Dt DI>
+__device__ __forceinline__ float raw_value_at(const uint4 &q, int e) {
+    if constexpr (DI == Dt::BF16) {
+        const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
+        return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+    } else {
+        return __uint_as_float(e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w);
+    }
+}
+
+template <Dt DI>
+__device__ __forceinline__ uint32_t raw_bits_at(const uint4 &q, int e) {
+    if constexpr (DI == Dt::BF16) {
+        const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
+        return (e & 1) ? w >> 16 : w & 0xffffu;
+    } else {
+        return e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
+    }
+}
+
+// Warp-wide sort of one float per lane, largest in lane 0 (bitonic network
+// on shuffles; no NaN among the inputs).
+__device__ __forceinline__ float warp_sort_desc(float v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool lower = (lane & stride) == 0, desc = (lane & size) == 0;
+            v = lower == desc ? fmaxf(v, o) : fminf(v, o);
+        }
+    }
+    return v;
+}
+
 template <Dt DI, int U>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
-    using Key = typename std::conditional<DI == Dt::BF16, uint16_t, uint32_t>::type;
+__global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a) {
+    using Raw = typename std::conditional<DI == Dt::BF16, uint16_t, uint32_t>::type;
     constexpr int KB = DI == Dt::BF16 ? 16 : 32;  // key bits
     constexpr int PASSES = KB / 8;
-    constexpr uint32_t kKeyInf = DI == Dt::BF16 ? 0xff80u : 0xff800000u;  // NaN keys lie above
     extern __shared__ __align__(16) unsigned char smem[];
-    Key *keys = reinterpret_cast<Key *>(smem);              // the piece, as keys
-    uint64_t *sortbuf = reinterpret_cast<uint64_t *>(smem);  // reuses the piece region
-    uint32_t *hist_w = reinterpret_cast<uint32_t *>(smem + a.region0);
-    uint32_t *hist_pub = hist_w + kWarps * 256;            // [2][256]
-    uint64_t *cand = reinterpret_cast<uint64_t *>(hist_pub + 2 * 256);
-    __shared__ float s_red[kWarps];
+    Raw *piece = reinterpret_cast<Raw *>(smem);             // the piece, raw
+    uint64_t *words = reinterpret_cast<uint64_t *>(smem);    // reuses the piece region
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + a.region0);
+    uint32_t *hist_pub = hist + 256;                         // [2][256]
+    uint64_t *list = reinterpret_cast<uint64_t *>(hist_pub + 2 * 256);
+    uint64_t *cand = list + kTopkListCap;
+    __shared__ float s_red[kWarps], s_gw[kWarps];
     __shared__ uint32_t s_scan[kWarps];
-    __shared__ float pub_d;
-    __shared__ uint32_t pub_kmax, pub_eq, pub_cand, s_bin, s_krem;
+    __shared__ float s_ez[kTopkRankMaxK];
+    __shared__ float pub_m, pub_d;
+    __shared__ uint32_t pub_n, pub_cand, list_n, s_bin, s_krem;
+    __shared__ float s_rm[kTopkMaxCluster], s_rd[kTopkMaxCluster];
+    __shared__ uint32_t s_rn[kTopkMaxCluster], s_off[kTopkMaxCluster + 1];
+    __shared__ uint64_t s_top;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cs = a.cs;
     const uint32_t rank = cluster_ctarank();
-    const int64_t row = blockIdx.x / cs;
+    const int64_t row = blockIdx.x / (uint32_t)cs;
     const int64_t e0 = (int64_t)rank * a.chunk;
     const int64_t e1 = e0 + a.chunk < a.N ? e0 + a.chunk : a.N;
     const int n = e1 > e0 ? (int)(e1 - e0) : 0;  // elements of this CTA's piece
-    const Key *xrow = reinterpret_cast<const Key *>(a.x) + row * a.N;
-    uint32_t *hw = hist_w + warp * 256;
+    const Raw *xrow = reinterpret_cast<const Raw *>(a.x) + row * a.N;
+    const int64_t k = a.k;
     const uint32_t inv = 0xffffffffu;
-    auto candidate = [&](uint32_t key, int i) {  // (key, column) -> sort word, kept
-        const uint32_t pos = atomicAdd(&pub_cand, 1u);
-        if (pos < (uint32_t)a.k)  // at most k by construction; never past the list
-            cand[pos] = ((uint64_t)key << 32) | (uint64_t)(inv - (uint32_t)(e0 + i));
+    // (key, column) <-> one 64-bit word ordered by key, then by smaller column
+    auto word = [&](uint32_t key, int64_t col) {
+        return ((uint64_t)key << 32) | (uint64_t)(inv - (uint32_t)col);
     };
-    // every key of the piece, with its element index, in any order
-    auto sweep = [&](auto &&f) {
+    auto candidate = [&](uint64_t w) {
+        const uint32_t pos = atomicAdd(&pub_cand, 1u);
+        if (pos < (uint32_t)k) cand[pos] = w;  // at most k by construction
+    };
+    // every element of the piece as (value, raw bits, column), in any order
+    auto sweep_piece = [&](auto &&f) {
         if constexpr (U > 1) {
-            const uint4 *kv = reinterpret_cast<const uint4 *>(keys);
+            const uint4 *pv = reinterpret_cast<const uint4 *>(piece);
             for (int i = tid; i < n / U; i += kTopkThreads) {
-                const uint4 q = kv[i];
+                const uint4 q = pv[i];
 #pragma unroll
-                for (int e = 0; e < U; ++e) f(key_at<DI>(q, e), i * U + e);
+                for (int e = 0; e < U; ++e) f(raw_value_at<DI>(q, e), raw_bits_at<DI>(q, e), e0 + i * U + e);
             }
         } else {
-            for (int i = tid; i < n; i += kTopkThreads) f((uint32_t)keys[i], i);
+            for (int i = tid; i < n; i += kTopkThreads) {
+                const uint32_t b = piece[i];
+                f(raw_to_f32(b, DI), b, e0 + i);
+            }
         }
     };
 
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) hist_w[w * 256 + tid] = 0u;
-    if (tid == 0) pub_cand = 0;
-    __syncthreads();
+    if (tid == 0) {
+        pub_cand = 0;
+        list_n = 0;
+    }
     pdl_wait();
 
-    // ---- load: raw values -> keys in shared memory (the row is read from HBM
-    //      once), with pass 0 on the way: the largest key of a number and the
-    //      histogram of the top digit
-    uint32_t kmax = 0;  // 0: no number seen
-    auto visit0 = [&](uint32_t key) {
-        if (key <= kKeyInf && key > kmax) kmax = key;
-        atomicAdd(&hw[key >> (KB - 8)], 1u);
-    };
+    // ---- load the piece (the row is read from HBM once, every copy in
+    //      flight at once) and take each thread's largest number (NaN skipped)
+    float tmax = -INFINITY;
     if constexpr (U > 1) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(xrow + e0);
-        uint4 *dst = reinterpret_cast<uint4 *>(keys);
+        const char *src = reinterpret_cast<const char *>(xrow + e0);
+        uint4 *pv = reinterpret_cast<uint4 *>(piece);
         const int nv = n / U;  // n is a multiple of U on the vector path
-        for (int i0 = tid; i0 < nv; i0 += 4 * kTopkThreads) {
-            uint4 q[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = i0 + j * kTopkThreads;
-                q[j] = i < nv ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < nv; i += kTopkThreads) cp_async16(smem_u32(pv + i), src + (int64_t)i * 16);
+        cp_async_wait_all();  // this thread's own copies; it reads only those here
+        if constexpr (DI == Dt::BF16) {
+            uint32_t mx = 0xff80ff80u;  // (-inf, -inf)
+            for (int i = tid; i < nv; i += kTopkThreads) {
+                const uint4 q = pv[i];
+                mx = max_bf16x2(mx, max_bf16x2(max_bf16x2(q.x, q.y), max_bf16x2(q.z, q.w)));
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = i0 + j * kTopkThreads;
-                if (i < nv) {
-                    const uint4 kq = keys_of<DI>(q[j]);
-                    dst[i] = kq;
-#pragma unroll
-                    for (int e = 0; e < U; ++e) visit0(key_at<DI>(kq, e));
-                }
+            tmax = fmaxf(bf16_lo(mx), bf16_hi(mx));
+        } else {
+            for (int i = tid; i < nv; i += kTopkThreads) {
+                const uint4 q = pv[i];
+                tmax = fmaxf(tmax, fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                         fmaxf(__uint_as_float(q.z), __uint_as_float(q.w))));
             }
         }
     } else {
         for (int i = tid; i < n; i += kTopkThreads) {
-            const uint32_t key = topk_key(xrow[e0 + i], DI);
-            keys[i] = (Key)key;
-            visit0(key);
+            const Raw b = xrow[e0 + i];
+            piece[i] = b;
+            tmax = fmaxf(tmax, raw_to_f32(b, DI));
         }
     }
 
-    // ---- radix selection of the k-th largest key, with the row's m and d
-    uint32_t prefix = 0;  // the chosen digits so far
-    uint32_t krem = (uint32_t)a.k;
-    float m = -FLT_MAX, d = 0.f;
-#pragma unroll 1
-    for (int p = 0; p < PASSES; ++p) {
-        const int shift = KB - 8 * (p + 1);
-        if (p == 0) {
-            kmax = block_max_u32(kmax, s_scan);  // also orders the histogram atomics
-            if (tid == 0) pub_kmax = kmax;
-        } else {
+    // ---- a lower bound g of the row's k-th largest element.  With
+    //      q = ceil(k/8), take in each warp the q-th largest lane maximum and
+    //      let g be the smallest of those: at least 8q >= k threads hold a
+    //      number >= g, so nothing below g is among the k largest (a NaN
+    //      ranks above every number and is always kept).  k > 256: no bound.
+    const uint32_t qk = (uint32_t)((k + kWarps - 1) / kWarps);
+    const float sorted = warp_sort_desc(tmax);
+    const float gw = __shfl_sync(0xffffffffu, sorted, (int)((qk <= 32 ? qk : 32) - 1));
+    if (lane == 0) s_gw[warp] = gw;
+    const float cmax = block_max_f(tmax, s_red);  // its barriers publish s_gw too
+    float g = -INFINITY;
+    if (qk <= 32) {
+        g = INFINITY;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) hist_w[w * 256 + tid] = 0u;
+        for (int w = 0; w < kWarps; ++w) g = fminf(g, s_gw[w]);
+    }
+
+    // ---- one sweep: this CTA's (m, d) for the log-sum-exp, and the elements
+    //      not below g, as (key, column) words, into a short list
+    const float mc = fmaxf(cmax, -FLT_MAX);
+    float dt = 0.f;
+    sweep_piece([&](float v, uint32_t bits, int64_t col) {
+        dt += exp_shifted(v, mc);
+        if (!(v < g)) {
+            const uint32_t pos = atomicAdd(&list_n, 1u);
+            if (pos < (uint32_t)kTopkListCap) list[pos] = word(topk_key(bits, DI), col);
+        }
+    });
+    dt = block_sum_f(dt, s_red);  // also orders the list appends
+    const uint32_t nl = list_n;
+    if (tid == 0) {
+        pub_m = mc;
+        pub_d = dt;
+        pub_n = nl;
+    }
+
+    // ---- exchange: the row's (m, d) by the merge of the CTAs' (m, d), and
+    //      the lists' lengths (thread r reads CTA r's, all at once)
+    cluster_sync_all();
+    if (tid < cs) {
+        s_rm[tid] = ld_dsmem_f32(mapa_shared(smem_u32(&pub_m), tid));
+        s_rd[tid] = ld_dsmem_f32(mapa_shared(smem_u32(&pub_d), tid));
+        s_rn[tid] = ld_dsmem_u32(mapa_shared(smem_u32(&pub_n), tid));
+    }
+    __syncthreads();
+    float m = -FLT_MAX, d = 0.f;
+    uint32_t over = 0, total = 0;
+    for (int r = 0; r < cs; ++r) {
+        m = fmaxf(m, s_rm[r]);
+        over |= s_rn[r] > (uint32_t)kTopkListCap;
+        total += s_rn[r] < (uint32_t)kTopkListCap ? s_rn[r] : (uint32_t)kTopkListCap;
+    }
+    for (int r = 0; r < cs; ++r) d += s_rd[r] * expf(s_rm[r] - m);
+    if (rank == 0 && a.lse != nullptr && tid == 0) a.lse[row] = m + logf(d);
+
+    auto value_at = [&](uint32_t j) {  // the row's own value (an index outside
+        // the row could only come from a selection that found fewer than k
+        // candidates: reported as NaN, never read)
+        return j < (uint32_t)a.N ? raw_to_f32(xrow[j], DI) : __uint_as_float(0x7fc00000u);
+    };
+    auto store = [&](int64_t t, uint32_t j, float p) {
+        a.values[row * k + t] = value_at(j);
+        a.indices[row * k + t] = j < (uint32_t)a.N ? (int64_t)j : -1;
+        if (a.probs != nullptr) a.probs[row * k + t] = p;
+    };
+    // Radix selection of the k-th largest key T among keys delivered by
+    // `each` (8 bits per pass from the top).  `merge` turns this CTA's
+    // histogram into the one the choice is made from (the cluster's sum, or
+    // the CTA's own); returns T and leaves in krem how many keys equal to T
+    // belong to the k largest.
+    uint32_t krem = (uint32_t)k;
+    auto radix_select = [&](auto &&each, auto &&merge) {
+        uint32_t prefix = 0;
+        krem = (uint32_t)k;
+#pragma unroll 1
+        for (int p = 0; p < PASSES; ++p) {
+            const int shift = KB - 8 * (p + 1);
+            hist[tid] = 0u;
             __syncthreads();
-            float acc = 0.f;
-            sweep([&](uint32_t key, int) {
-                if (p == 1) acc += exp_shifted(key_value<DI>(key), m);
-                if ((key >> (shift + 8)) == prefix) atomicAdd(&hw[(key >> shift) & 255u], 1u);
+            each([&](uint32_t key, int64_t) {
+                if (p == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
             });
-            if (p == 1) {
-                acc = block_sum_f(acc, s_red);
-                if (tid == 0) pub_d = acc;
+            __syncthreads();
+            const uint32_t H = merge(hist[tid]);
+            __syncthreads();
+            // S_b = keys in play with digit >= b, an inclusive scan in
+            // descending digit order: thread t takes digit 255 - t
+            hist[255 - tid] = H;
+            __syncthreads();
+            const uint32_t Hr = hist[tid];
+            const uint32_t S = block_inclusive_scan(Hr, s_scan);
+            if (S >= krem && S - Hr < krem) {
+                s_bin = 255u - (uint32_t)tid;
+                s_krem = krem - (S - Hr);
+            }
+            __syncthreads();
+            prefix = (prefix << 8) | s_bin;
+            krem = s_krem;
+            __syncthreads();
+        }
+        return prefix;
+    };
+
+    bool in_cand = false;  // CTA 0's k words: in `cand` (short path) or in `words`
+    if (!over && total <= a.region0 / 8) {
+        // ---- the short path: the union of the lists holds every element at
+        //      or above the k-th largest (each CTA's bound lies below it).
+        //      CTA 0 gathers the union and selects from it alone.
+        if (rank == 0) {
+            // word i of the union: list of CTA r, entry i - s_off[r]
+            if (tid == 0) {
+                s_off[0] = 0;
+                for (int r = 0; r < cs; ++r) s_off[r + 1] = s_off[r] + s_rn[r];
+            }
+            __syncthreads();
+            for (uint32_t i0 = tid; i0 < total; i0 += 4 * kTopkThreads) {
+                uint64_t v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t i = i0 + j * kTopkThreads;
+                    v[j] = 0ull;
+                    if (i < total) {
+                        int r = 0;
+                        while (i >= s_off[r + 1]) ++r;
+                        v[j] = ld_dsmem_u64(mapa_shared(smem_u32(list + (i - s_off[r])), r));
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t i = i0 + j * kTopkThreads;
+                    if (i < total) words[i] = v[j];
+                }
+            }
+        }
+        cluster_sync_all();  // no CTA leaves while CTA 0 reads its list
+        if (rank != 0) {
+            pdl_trigger();
+            return;
+        }
+        __syncthreads();
+        auto each_u = [&](auto &&f) {
+            for (uint32_t i = tid; i < total; i += kTopkThreads) f((uint32_t)(words[i] >> 32), (int64_t)i);
+        };
+        const uint32_t T = radix_select(each_u, [](uint32_t h) { return h; });
+        // keys above T, and the krem largest words among those equal to T
+        // (equal keys: the smaller columns; every word differs).  The equal
+        // words are gathered into `list` (free now) and ranked among
+        // themselves.
+        if (tid == 0) list_n = 0;
+        __syncthreads();
+        for (uint32_t i = tid; i < total; i += kTopkThreads) {
+            const uint64_t w = words[i];
+            const uint32_t key = (uint32_t)(w >> 32);
+            if (key > T) candidate(w);
+            if (key == T) {
+                const uint32_t pos = atomicAdd(&list_n, 1u);
+                if (pos < (uint32_t)kTopkListCap) list[pos] = w;
+            }
+        }
+        __syncthreads();
+        const uint32_t ne = list_n;
+        if (ne <= (uint32_t)kTopkListCap) {
+            for (uint32_t i = tid; i < ne; i += kTopkThreads) {
+                const uint64_t w = list[i];
+                uint32_t larger = 0;
+                for (uint32_t j = 0; j < ne; ++j) larger += list[j] > w;
+                if (larger < krem) candidate(w);
+            }
+        } else {  // too many equal keys to gather: rank them over the union
+            for (uint32_t i = tid; i < total; i += kTopkThreads) {
+                const uint64_t w = words[i];
+                if ((uint32_t)(w >> 32) != T) continue;
+                uint32_t larger = 0;
+                for (uint32_t j = 0; j < total; ++j) larger += (uint32_t)(words[j] >> 32) == T && words[j] > w;
+                if (larger < krem) candidate(w);
+            }
+        }
+        in_cand = true;
+    } else {
+        // ---- otherwise the cluster selects together, over the lists (or,
+        //      when a list overflowed, over the whole pieces).  Published
+        //      histograms alternate between two buffers per exchange, so a
+        //      CTA never overwrites one another CTA may still read.
+        const bool full = over != 0;  // cluster-uniform
+        auto each = [&](auto &&f) {
+            if (full) {
+                sweep_piece([&](float, uint32_t bits, int64_t col) { f(topk_key(bits, DI), col); });
             } else {
+                for (uint32_t i = tid; i < nl; i += kTopkThreads) {
+                    const uint64_t w = list[i];
+                    f((uint32_t)(w >> 32), (int64_t)(inv - (uint32_t)w));
+                }
+            }
+        };
+        int xb = 0;
+        uint32_t *pub = nullptr;
+        auto cluster_merge = [&](uint32_t h) {
+            pub = hist_pub + xb * 256;
+            pub[tid] = h;
+            xb ^= 1;
+            cluster_sync_all();
+            uint32_t H = 0;
+            for (int r = 0; r < cs; ++r) H += ld_dsmem_u32(mapa_shared(smem_u32(pub + tid), r));
+            return H;
+        };
+        const uint32_t T = radix_select(each, cluster_merge);
+        // the last histograms count, per CTA, the keys equal to T: bin (T & 255)
+        uint32_t eq_before = 0;
+        for (int r = 0; r < (int)rank; ++r)
+            eq_before += ld_dsmem_u32(mapa_shared(smem_u32(pub + (T & 255u)), r));
+        const uint32_t eq_here = pub[T & 255u];
+        const uint32_t quota = krem > eq_before ? (krem - eq_before < eq_here ? krem - eq_before : eq_here) : 0u;
+        const bool all_eq = quota == eq_here;
+        each([&](uint32_t key, int64_t col) {
+            if (key > T || (all_eq && key == T && quota > 0)) candidate(word(key, col));
+        });
+        if (!all_eq && quota > 0) {
+            // a partial share (one CTA of the row at most): the lowest-indexed
+            // equal keys.  Each thread walks a contiguous range of the piece,
+            // so index order is (thread, position): count, scan, take in order.
+            const int L = (n + kTopkThreads - 1) / kTopkThreads;
+            const int j0 = tid * L < n ? tid * L : n, j1 = j0 + L < n ? j0 + L : n;
+            uint32_t c = 0;
+            for (int j = j0; j < j1; ++j) c += topk_key(piece[j], DI) == T;
+            const uint32_t incl = block_inclusive_scan(c, s_scan);
+            uint32_t r = incl - c;  // equal keys before this thread's range
+            for (int j = j0; j < j1 && r < quota; ++j)
+                if (topk_key(piece[j], DI) == T) {
+                    candidate(word(T, e0 + j));
+                    ++r;
+                }
+        }
+        cluster_sync_all();  // every CTA's candidates are complete
+        if (rank == 0) {
+            uint32_t off = 0;
+            for (int r = 0; r < cs; ++r) {
+                uint32_t cnt = ld_dsmem_u32(mapa_shared(smem_u32(&pub_cand), r));
+                cnt = off + cnt <= (uint32_t)k ? cnt : (off < (uint32_t)k ? (uint32_t)k - off : 0u);
+                copy_words(words + off, mapa_shared(smem_u32(cand), r), cnt);
+                off += cnt;
+            }
+        }
+        cluster_sync_all();  // no CTA leaves while CTA 0 reads its candidates
+        if (rank != 0) {
+            pdl_trigger();
+            return;
+        }
+    }
+    __syncthreads();
+    if (in_cand) {
+        for (int i = tid; i < k; i += kTopkThreads) words[i] = cand[i];
+        __syncthreads();
+    }
+
+    // ---- CTA 0 writes the k words in order: values re-read from the row,
+    //      columns, the softmax of the k values (largest first, so v0 is their
+    //      maximum), summed in output order
+    if (k <= kTopkRankMaxK) {
+        // output position = the number of larger words (all words differ)
+        int64_t t = 0;
+        uint64_t w = 0;
+        if (tid < k) {
+            w = words[tid];
+            for (int j = 0; j < k; ++j) t += words[j] > w;
+            if (t == 0) s_top = w;
+        }
+        __syncthreads();
+        const float v0 = key_value<DI>((uint32_t)(s_top >> 32));  // the largest value
+        if (tid < k) s_ez[t] = expf(key_value<DI>((uint32_t)(w >> 32)) - v0);
+        __syncthreads();
+        const float rz = __frcp_rn(block_sum_f(tid < k ? s_ez[tid] : 0.f, s_red));
+        if (tid < k) store(t, inv - (uint32_t)w, s_ez[t] * rz);
+    } else {
+        // a bitonic network on a.sort_n >= k words (zero words sort last)
+        for (int i = (int)k + tid; i < a.sort_n; i += kTopkThreads) words[i] = 0ull;
+        __syncthreads();
+        for (int size = 2; size <= a.sort_n; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < a.sort_n / 2; i += kTopkThreads) {
+                    const int lo = 2 * i - (i & (stride - 1));
+                    const int hi = lo + stride;
+                    const uint64_t A = words[lo], B = words[hi];
+                    if ((lo & size) == 0 ? A < B : A > B) {
+                        words[lo] = B;
+                        words[hi] = A;
+                    }
+                }
                 __syncthreads();
             }
         }
-        uint32_t h = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) h += hist_w[w * 256 + tid];
-        uint32_t *pub = hist_pub + (p & 1) * 256;
-        pub[tid] = h;
-        cluster_sync_all();
-        // the cluster's histogram and statistics, read in rank order
-        uint32_t H = 0, km = 0;
-        float ds = 0.f;
-        for (int r = 0; r < cs; ++r) {
-            H += ld_dsmem_u32(mapa_shared(smem_u32(pub + tid), r));
-            if (p == 0) {
-                const uint32_t o = ld_dsmem_u32(mapa_shared(smem_u32(&pub_kmax), r));
-                km = o > km ? o : km;
-            }
-            if (p == 1) ds += ld_dsmem_f32(mapa_shared(smem_u32(&pub_d), r));
-        }
-        if (p == 0) m = km == 0 ? -FLT_MAX : fmaxf(key_value<DI>(km), -FLT_MAX);
-        if (p == 1) d = ds;
-        // S_b = elements in play with digit >= b, an inclusive scan in
-        // descending digit order: thread t takes digit 255 - t.  (The
-        // per-warp histograms are free again: the cluster barrier above
-        // follows every thread's reads of them.)
-        hist_w[255 - tid] = H;
-        __syncthreads();
-        const uint32_t Hr = hist_w[tid];
-        const uint32_t S = block_inclusive_scan(Hr, s_scan);
-        if (S >= krem && S - Hr < krem) {
-            s_bin = 255u - (uint32_t)tid;
-            s_krem = krem - (S - Hr);
-        }
-        __syncthreads();
-        prefix = (prefix << 8) | s_bin;
-        krem = s_krem;
-        __syncthreads();
-    }
-    const uint32_t T = prefix;  // key of the k-th largest element
-    // krem: how many elements equal to T are taken (the lowest-indexed ones)
-
-    // ---- gather: every key above T; the count of keys equal to T
-    uint32_t eqc = 0;
-    sweep([&](uint32_t key, int i) {
-        if (key > T) candidate(key, i);
-        eqc += key == T;
-    });
-    eqc = block_inclusive_scan(eqc, s_scan);  // thread 255 holds the CTA's count
-    if (tid == kTopkThreads - 1) pub_eq = eqc;
-    cluster_sync_all();
-    uint32_t eq_before = 0;
-    for (int r = 0; r < (int)rank; ++r) eq_before += ld_dsmem_u32(mapa_shared(smem_u32(&pub_eq), r));
-    const uint32_t eq_here = pub_eq;
-    const uint32_t quota = krem > eq_before ? (krem - eq_before < eq_here ? krem - eq_before : eq_here) : 0u;
-    if (quota == eq_here && quota > 0) {
-        sweep([&](uint32_t key, int i) {
-            if (key == T) candidate(key, i);
-        });
-    } else if (quota > 0) {
-        // a partial share (one CTA of the row at most): the lowest-indexed
-        // equal keys.  Each thread walks a contiguous range of the piece, so
-        // index order is (thread, position): count, scan, take in order.
-        const int L = (n + kTopkThreads - 1) / kTopkThreads;
-        const int j0 = tid * L, j1 = j0 + L < n ? j0 + L : n;
-        uint32_t c = 0;
-        for (int j = j0; j < j1; ++j) c += (uint32_t)keys[j] == T;
-        const uint32_t incl = block_inclusive_scan(c, s_scan);
-        uint32_t r = incl - c;  // equal keys before this thread's range
-        for (int j = j0; j < j1 && r < quota; ++j)
-            if ((uint32_t)keys[j] == T) {
-                candidate(T, j);
-                ++r;
-            }
-    }
-    cluster_sync_all();  // every CTA's candidates are complete
-
-    if (rank == 0) {
-        // pull the k candidates (rank order), pad the network with zero words
-        // (below every real key), then sort descending
-        uint32_t off = 0;
-        for (int r = 0; r < cs; ++r) {
-            const uint32_t cnt = ld_dsmem_u32(mapa_shared(smem_u32(&pub_cand), r));
-            const uint32_t src = mapa_shared(smem_u32(cand), r);
-            for (uint32_t i = tid; i < cnt && off + i < (uint32_t)a.sort_n; i += kTopkThreads)
-                sortbuf[off + i] = ld_dsmem_u64(src + i * 8);
-            off += cnt;
-        }
-        for (int i = (int)a.k + tid; i < a.sort_n; i += kTopkThreads) sortbuf[i] = 0ull;
-    }
-    cluster_sync_all();  // no CTA leaves while CTA 0 reads its candidates
-    if (rank != 0) {
-        pdl_trigger();
-        return;
-    }
-    __syncthreads();
-    for (int size = 2; size <= a.sort_n; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < a.sort_n / 2; i += kTopkThreads) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const uint64_t A = sortbuf[lo], B = sortbuf[hi];
-                const bool desc = (lo & size) == 0;
-                if (desc ? A < B : A > B) {
-                    sortbuf[lo] = B;
-                    sortbuf[hi] = A;
-                }
-            }
-            __syncthreads();
-        }
-    }
-
-    // ---- outputs: values re-read from the row (L2), indices, softmax of the
-    //      k values (largest first, so v0 is their maximum), lse.  (An index
-    //      outside the row can only come from a selection that did not find k
-    //      candidates: it is reported as -1 with a NaN value, never read.)
-    const int64_t k = a.k;
-    auto value_at = [&](uint32_t j) {
-        return j < (uint32_t)a.N ? raw_to_f32(xrow[j], DI) : __uint_as_float(0x7fc00000u);
-    };
-    const float v0 = value_at(inv - (uint32_t)sortbuf[0]);
-    float zsum = 0.f;
-    for (int t = tid; t < k; t += kTopkThreads) {
-        const uint32_t j = inv - (uint32_t)sortbuf[t];
-        const float v = value_at(j);
-        a.values[row * k + t] = v;
-        a.indices[row * k + t] = j < (uint32_t)a.N ? (int64_t)j : -1;
-        zsum += expf(v - v0);
-    }
-    if (a.probs != nullptr) {
-        zsum = block_sum_f(zsum, s_red);
+        const float v0 = key_value<DI>((uint32_t)(words[0] >> 32));  // the largest value
+        float z = 0.f;
+        for (int t = tid; t < k; t += kTopkThreads) z += expf(key_value<DI>((uint32_t)(words[t] >> 32)) - v0);
+        const float rz = __frcp_rn(block_sum_f(z, s_red));
         for (int t = tid; t < k; t += kTopkThreads)
-            a.probs[row * k + t] = expf(value_at(inv - (uint32_t)sortbuf[t]) - v0) / zsum;
+            store(t, inv - (uint32_t)words[t], expf(key_value<DI>((uint32_t)(words[t] >> 32)) - v0) * rz);
     }
-    if (a.lse != nullptr && tid == 0) a.lse[row] = m + logf(d);
     pdl_trigger();
 }
 

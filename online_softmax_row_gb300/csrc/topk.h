@@ -28,11 +28,14 @@ constexpr int kTopkThreads = 256;
 constexpr int64_t kTopkMaxK = 1024;
 constexpr int64_t kTopkMaxPieceBytes = 192 << 10;  // largest piece a CTA caches
 constexpr int kTopkMaxCluster = 16;
+constexpr int kTopkListCap = 1024;  // keys at or above a CTA's bound kept in a short list
+constexpr int64_t kTopkRankMaxK = 256;  // k up to this: outputs placed by counting, no sort
+constexpr int64_t kTopkMinWords = 2048;  // the piece region holds at least this many 8-byte words
 
-// Dynamic shared memory of one CTA: piece (or sort buffer), per-warp
-// histograms, the published histogram (two buffers), the candidate list.
+// Dynamic shared memory of one CTA: piece (or sort buffer), the histogram,
+// the published histogram (two buffers), the short list, the candidates.
 inline size_t topk_smem_bytes(uint32_t region0, int64_t k) {
-    return (size_t)region0 + (size_t)(kTopkThreads / 32) * 256 * 4 + 2 * 256 * 4 + (size_t)k * 8;
+    return (size_t)region0 + 256 * 4 + 2 * 256 * 4 + (size_t)kTopkListCap * 8 + (size_t)k * 8;
 }
 
 template <Dt DI>
