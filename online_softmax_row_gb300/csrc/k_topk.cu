@@ -11,25 +11,31 @@
 // "两个融合算子：RMSNorm 与 online softmax" (daleiyang.github.io) §3 names for
 // top-k bucketing, here with shared-memory histograms.
 //
-// One thread-block cluster of cs CTAs per row; CTA r caches elements
-// [r * chunk, (r + 1) * chunk) of the row in shared memory as order-keys (so
-// the row is read from HBM once) and all passes below run over that copy:
-//   select  -- radix selection of the k-th largest key, 8 bits per pass from
-//              the top (2 passes for bfloat16, 4 for binary32; the first runs
-//              while the row is loaded): every CTA histograms the digit of its
-//              elements whose higher digits equal the chosen prefix, the cs
-//              histograms are summed through distributed shared memory, and
-//              every CTA picks the same bin;
-//   lse     -- the first pass also takes the row maximum m, the second the
-//              sum d of e^(x - m); lse = m + log d;
-//   gather  -- elements with key above the k-th largest key T are taken; of
-//              those equal to T the lowest-indexed ones are taken (a prefix
-//              over the cluster's CTAs; inside the one CTA whose share is
-//              partial, an in-order scan), exactly k in all;
-//   sort    -- CTA 0 pulls the k candidates of all CTAs, sorts them by (key
-//              descending, index ascending) with a bitonic network and writes
-//              values (re-read from the row), indices, probabilities and lse.
-// The result is unique (a total order), so it is deterministic.
+// One thread-block cluster of cs CTAs per row; CTA r copies elements
+// [r * chunk, (r + 1) * chunk) of the row into shared memory (cp.async: the
+// row is read from HBM once) and works on that copy:
+//   bound   -- each thread's largest number; per warp the ceil(k/8)-th
+//              largest of those, and g = the smallest over the warps: at
+//              least k elements of the CTA are >= g, so the row's k-th largest
+//              is >= g and nothing below g can be selected;
+//   sweep   -- one pass: the CTA's (m, d) = (max, sum of e^(x - max)) for the
+//              log-sum-exp, and every element not below g appended to a
+//              short list as a (key, column) word (keys: an order-preserving
+//              integer map, -0 as +0, NaN above every number; words order by
+//              key, then by smaller column, and all differ);
+//   merge   -- one cluster exchange: the row's (m, d) by the (m, d) merge of
+//              the CTAs' (lse = m + log d), and the lists' lengths;
+//   select  -- CTA 0 gathers the union of the lists (it holds every element
+//              at or above the k-th largest), finds the k-th largest key T by
+//              8-bit radix passes over it, takes the words above T and the
+//              largest of those equal to T, and writes them in order (values
+//              re-read from the row, columns, the softmax of the k values).
+// When a list overflows (k > 256 gives no bound; heavy ties at the bound) or
+// the union does not fit, the cluster selects together instead: radix passes
+// over the lists or the whole pieces with the histograms summed through
+// distributed shared memory each pass, and the equal keys shared out by a
+// prefix over the CTAs.  The result is unique (a total order), so it is
+// deterministic.
 #include <cuda_runtime.h>
 
 #include <type_traits>

@@ -157,3 +157,17 @@ def test_topk_workload_full_size():
     out = osr.row_topk(x.cuda(), w.k)
     torch.cuda.synchronize()
     check(x, w.k, *out, what=w.name)
+
+
+@pytest.mark.parametrize("spec", ["", "topk:cs=2"])
+def test_topk_constant_rows(spec):
+    # every element equal: the k smallest columns.  With two CTAs of 1000
+    # elements each the lists fit but all 2000 words tie (more than a
+    # gathered list holds); with one CTA the list itself overflows.
+    x = torch.full((3, 2000), 1.5, dtype=torch.bfloat16)
+    x[1] = -2.0
+    fn = lambda: osr.row_topk(x.cuda(), 50)
+    out = run_forced(spec, fn) if spec else fn()
+    torch.cuda.synchronize()
+    check(x, 50, *out, what=f"constant {spec or 'default'}")
+    assert out[1].cpu().tolist() == [list(range(50))] * 3
