@@ -110,11 +110,13 @@ int64_t pow2_at_least(int64_t v) {
     return c;
 }
 
-// Staged tier shape: the fewest CTAs per row whose pieces fit 96 KiB (or,
-// failing that, 200 KiB), raised until the grid has about three CTAs per SM
-// and rounded up to a power of two, which packs the GPCs better (measured:
-// 152064-element rows ran 13 % faster as 8 pieces than as 7).  force_cs: 0
-// decide.  Returns false if no piece within the limits holds the row.
+// Staged tier shape.  Few rows (three CTAs per SM would need 8 or more per
+// row): 12 CTAs per row, 16 for one or two rows.  Otherwise the fewest CTAs
+// whose pieces fit 96 KiB (or, failing that, 200 KiB), raised toward three
+// CTAs per SM, at least 8 for rows of 192 KiB or more, and rounded up to a
+// power of two, which packs the GPCs better (measured: 152064-element rows
+// ran 13 % faster as 8 pieces than as 7).  force_cs: 0 decide.  Returns
+// false if no piece within the limits holds the row.
 bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, int64_t force_cs, Plan *p) {
     const int64_t row_bytes = nunits * 16;
     int64_t cs = force_cs;
@@ -122,12 +124,25 @@ bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, int64_t f
         int64_t need = cdiv(row_bytes, kStagedPreferBytes);
         if (need > max_cluster) need = cdiv(row_bytes, kStagedMaxSmem - 128);
         int64_t fill = cdiv(3 * (int64_t)sms, M);
-        const int64_t most = cdiv(nunits, kStagedThreads);
-        if (fill > most) fill = most;
-        if (fill > max_cluster) fill = max_cluster;
-        cs = need > fill ? need : fill;
-        const int64_t c2 = pow2_at_least(cs);
-        if (c2 <= max_cluster && cdiv(nunits, c2) >= kStagedThreads / 4) cs = c2;
+        const int64_t most = cdiv(nunits, kStagedThreads);  // >= one unit per thread
+        if (fill >= 8 && need <= 12) {
+            // few rows: spread each row wide.  Measured on 1..64 rows of 64 Ki
+            // to 152 Ki elements: 16 CTAs for one or two rows, 12 otherwise
+            // (5-18 % faster than 8 or 16, e.g. 64 vocabulary rows 16.7 ->
+            // 15.8 us); larger clusters pay more than their extra bandwidth
+            cs = M <= 2 ? 16 : 12;
+            if (cs > max_cluster) cs = max_cluster;
+            if (cs > most) cs = most;
+        } else {
+            if (fill > most) fill = most;
+            if (fill > max_cluster) fill = max_cluster;
+            cs = need > fill ? need : fill;
+            // rows of 192 KiB and more: at least 8 pieces, so a wave holds
+            // enough CTAs (measured 4-10 % faster than 4 pieces at 128-256 rows)
+            if (row_bytes >= (192 << 10) && cs < 8) cs = 8;
+            const int64_t c2 = pow2_at_least(cs);
+            if (c2 <= max_cluster && cdiv(nunits, c2) >= kStagedThreads / 4) cs = c2;
+        }
     }
     if (cs < 1 || cs > max_cluster) return false;
     const int64_t chunk = cdiv(nunits, cs);

@@ -100,8 +100,8 @@ def test_bench_copy_validation(lib):
 
 @pytest.mark.parametrize("n,tier", [
     (1, "rows g=1"), (32, "rows g=2"), (128, "rows g=8"), (1024, "rows g=64"),
-    (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "staged cs=8"),
-    (152064, "staged cs=8"), (262144, "staged cs=16"), (1 << 20, "split"),
+    (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "staged cs=12"),
+    (152064, "staged cs=12"), (262144, "staged cs=12"), (1 << 20, "split"),
 ])
 def test_dispatch_tiers_softmax_f32(lib, n, tier):
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, n, "f32").startswith(tier)
@@ -110,7 +110,9 @@ def test_dispatch_tiers_softmax_f32(lib, n, tier):
 @pytest.mark.parametrize("m,n,want", [
     (2048, 32768, "staged cs=2 g=256 piece=65536B"),     # 2 pieces of 64 KiB
     (441, 152064, "staged cs=8 g=256 piece=76032B"),     # fewest pieces <= 96 KiB, 2^k
-    (64, 152064, "staged cs=8 g=256 piece=76032B"),      # few rows: spread over 8 CTAs
+    (128, 65536, "staged cs=8 g=256 piece=32768B"),      # rows >= 192 KiB: at least 8
+    (64, 152064, "staged cs=12 g=256 piece=50688B"),     # few rows: spread over 12 CTAs
+    (8, 65536, "staged cs=12 g=256 piece=21856B"),
     (1, 32768, "staged cs=16 g=256 piece=8192B"),        # one row: spread over 16 CTAs
     (3, 800000, "staged cs=16 g=256 piece=200000B"),     # largest pieces
 ])
@@ -135,7 +137,7 @@ def test_dispatch_capacity_counts_cached_elements():
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "rows g=1024 ept=32 vec"
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 65536, "bf16").startswith("cluster cs=2")
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 32767, "bf16").startswith("cluster cs=2 g=1024 ept=16 scalar")
-    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("staged cs=8")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("staged cs=12")
 
 
 def test_dispatch_scalar_path_when_misaligned():

@@ -16,7 +16,7 @@ import torch
 import oracle
 import online_softmax_row_gb300 as osr
 import workloads
-from parity import bits16, to_oracle_input
+from parity import seed_of, bits16, to_oracle_input
 
 pytestmark = pytest.mark.gpu
 EPS = 1e-5
@@ -28,9 +28,6 @@ def gpu():
         pytest.skip("no CUDA device")
     osr.library()
 
-
-def seed_of(*k):
-    return abs(hash(tuple(k))) % (2 ** 31)
 
 
 def ln_case(M, H, dt, seed, lo=None, hi=None):

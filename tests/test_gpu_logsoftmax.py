@@ -8,7 +8,10 @@ binary64):
     <= 26 tree levels), which logf turns into an absolute error of the same
     size, plus one rounding each for x - m, log and the subtraction.  Values
     near 0 (a dominant row maximum) are bounded absolutely, not relatively.
-  log-softmax, bf16 out: within 1 bf16 ulp, as for softmax.
+  log-softmax, bf16 out: within 1 bf16 ulp, as for softmax, or, where the
+    binary32 error is the absolute one above (values near 0: a dominant
+    maximum gives -log d with d barely above 1), within 4e-6 + 1e-5 |ref|
+    plus one bf16 spacing.
   log-sum-exp: |gpu - ref| <= 4e-6 + 2e-7 |ref| (the same d error, plus the
     rounding of m + log d to binary32).
   argmax: exact, the first index of the maximum on ties."""
@@ -21,7 +24,7 @@ import torch
 import oracle
 import online_softmax_row_gb300 as osr
 import workloads
-from parity import check_bf16, check_f32_abs, to_oracle_input
+from parity import seed_of, check_bf16, check_f32_abs, to_oracle_input
 
 pytestmark = pytest.mark.gpu
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -34,9 +37,6 @@ def gpu():
     osr.library()
 
 
-def seed_of(*k):
-    return abs(hash(tuple(k))) % (2 ** 31)
-
 
 def case(M, N, dt, seed, sigma=4.0):
     return workloads.softmax_inputs(M, N, dt, sigma=sigma, shift_rows=M // 3, seed=seed)["x"]
@@ -47,7 +47,7 @@ def check_log(x_cpu, y):
     if y.dtype == torch.float32:
         check_f32_abs(y, ref, 4e-6, 1e-5, "log-softmax")
     else:
-        check_bf16(y, ref, "log-softmax")
+        check_bf16(y, ref, "log-softmax", atol=4e-6, rtol=1e-5)
 
 
 def check_lse(x_cpu, lse, am):

@@ -13,7 +13,7 @@ import torch
 import oracle
 import online_softmax_row_gb300 as osr
 import workloads
-from parity import (bits16, check_bf16, check_f32, check_out, check_row_max_and_argmax,
+from parity import (seed_of, bits16, check_bf16, check_f32, check_out, check_row_max_and_argmax,
                     to_oracle_input)
 
 pytestmark = pytest.mark.gpu
@@ -33,9 +33,6 @@ def gpu():
     osr.library()  # must be built: fail loudly otherwise
     torch.cuda.init()
 
-
-def seed_of(*k):
-    return abs(hash(tuple(k))) % (2 ** 31)
 
 
 def run_forced(spec, fn):
