@@ -261,8 +261,9 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
 // Log-sum-exp / argmax geometry: the kernel streams, so any shape fits; it
 // only has to spread the rows.  Short rows: a group of g <= 32 lanes per row.
 // Otherwise one 256-thread CTA per row, and when there are fewer rows than
-// two per SM, a cluster of up to 8 CTAs per row (measured: 16-CTA clusters
-// were 70 % slower on 64 vocabulary rows).
+// two per SM, a cluster of CTAs per row (sizes below; 16-CTA clusters were
+// 70 % slower on 64 vocabulary rows).  OSR_FORCE_KERNEL="lse:cs=<n>" picks
+// the cluster size (tests).
 struct LsePlan {
     int g = 1;
     int cs = 1;
@@ -283,11 +284,16 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     }
     lp.g = 256;
     int64_t cs = 1;
-    if (M < 2 * (int64_t)sms) {
-        cs = pow2ceil(cdiv(4 * (int64_t)sms, M));
+    const char *force = getenv("OSR_FORCE_KERNEL");
+    int64_t fcs = 0;
+    if (force && strncmp(force, "lse", 3) == 0 && parse_kv(force, "cs", &fcs) && fcs >= 1 && fcs <= 16) {
+        cs = fcs;  // a forced cluster size (tests)
+    } else if (M < 2 * (int64_t)sms) {
+        // measured on 152064-element rows: 10 CTAs per row for up to 16 rows
+        // (18 % faster than 8), 4 for more (8 % faster than 8 at 64 rows)
+        cs = M <= 16 ? 10 : 4;
         const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
         if (cs > most) cs = most;
-        if (cs > 8) cs = 8;
         if (cs < 1) cs = 1;
     }
     lp.cs = (int)cs;
@@ -408,9 +414,8 @@ osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_
 
 // Top-k geometry: one cluster of cs CTAs per row, each caching a piece of
 // the row (at most kTopkMaxPieceBytes) in shared memory.  The fewest CTAs
-// that hold the row, raised so that few rows still spread over the SMs
-// (powers of two up to 8, or up to 16 when even 16 per row leave SMs idle),
-// but never so far that a CTA gets less than one vector per thread.
+// that hold the row, raised by the row count (below), but never so far that
+// a CTA gets less than one vector per thread.
 // OSR_FORCE_KERNEL="topk:cs=<n>" picks cs (tests).
 struct TopkPlan {
     int cs = 1;
@@ -437,9 +442,11 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
         cs = fcs;
         tp->forced = true;
     } else {
-        int64_t fill = pow2_at_least(cdiv(2 * (int64_t)sms, M > 0 ? M : 1));
-        const int64_t cap = M * 16 <= sms ? 16 : 8;
-        if (fill > cap) fill = cap;
+        // measured on 1-256 rows of 152064 elements: 12 CTAs per row for up to
+        // 16 rows (7-11 % faster than 16), 4 up to 96 rows (10 % faster than 8
+        // at 64), 6 beyond; never fewer than the row needs, and never so many
+        // that a CTA gets less than one vector per thread
+        const int64_t fill = M <= 16 ? 12 : M <= 96 ? 4 : 6;
         if (fill > cs) cs = fill;
         while (cs > cs_min && cdiv(N, cs) < (int64_t)kTopkThreads * u) cs = cs / 2 > cs_min ? cs / 2 : cs_min;
     }

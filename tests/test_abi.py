@@ -187,7 +187,8 @@ def test_forced_kernel(monkeypatch):
 
 
 def test_logsumexp_plans_and_validation(lib):
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 1, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8192, 32000, "bf16") == "lse-rows g=256 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 100000, 32, "f32") == "lse-rows g=1 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOG_SOFTMAX, 64, 4096, "f32") == "rows g=256 ept=16 vec"
@@ -213,16 +214,19 @@ def test_layernorm_plans_and_validation(lib):
 
 def test_topk_plans_and_validation(lib, monkeypatch):
     D = osr.plan_describe
-    assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=8 piece=38016B vec"
-    assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=16 piece=19008B vec"   # one row: 16 CTAs
-    assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=8 piece=76032B vec"
+    assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
+    assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=12 piece=25344B vec"   # few rows: 12 CTAs
+    assert D(osr.OP_TOPK, 256, 152064, "bf16") == "topk cs=6 piece=50688B vec"
+    assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=4 piece=152064B vec"
     assert D(osr.OP_TOPK, 8, 1000, "bf16") == "topk cs=1 piece=2000B vec"       # short rows: one CTA
     assert D(osr.OP_TOPK, 3, 33, "bf16", vec_ok=False) == "topk cs=1 piece=66B scalar"
     assert D(osr.OP_TOPK, 1, 786432, "f32") == "topk cs=16 piece=196608B vec"   # largest row
     with pytest.raises(osr.OsrError):
         D(osr.OP_TOPK, 1, 786433, "f32")                                        # beyond 16 x 192 KiB
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "topk:cs=4")
-    assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "topk:cs=8")
+    assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=8 piece=38016B vec"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=16 vec"
     monkeypatch.delenv("OSR_FORCE_KERNEL")
     T = lib.osr_row_topk
     assert T(P, P * 8, P * 16, None, None, 0, 16, 4, F32, None) == 0            # M == 0

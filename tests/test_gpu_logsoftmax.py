@@ -155,3 +155,15 @@ def test_log_softmax_vocab_workload_full_size():
     y = osr.log_softmax_rows(x.cuda(), out_dtype=torch.float32)
     torch.cuda.synchronize()
     check_log(x, y)
+
+
+@pytest.mark.parametrize("cs", [2, 3, 10, 12, 16])
+def test_logsumexp_forced_cluster_sizes(cs):
+    x = case(6, 152064, "bf16", seed_of("lse-cs", cs))
+    os.environ["OSR_FORCE_KERNEL"] = f"lse:cs={cs}"
+    try:
+        lse, am = osr.row_logsumexp(x.cuda())
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["OSR_FORCE_KERNEL"]
+    check_lse(x, lse, am)
