@@ -26,11 +26,15 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * - Pointers named x, y, residual, gamma, out, row_max, row_sum are DEVICE
- *   pointers (memory the current CUDA device can read/write: cudaMalloc,
- *   cudaMallocAsync, managed memory, or a torch CUDA tensor's data_ptr()).
- *   The caller owns every buffer; the library keeps no pointer after the
- *   call returns.
+ * - Pointers named x, y, residual, gamma, beta, out, row_max, row_sum, lse,
+ *   values, ... are pointers the current CUDA device can read/write at that
+ *   address: device memory (cudaMalloc, cudaMallocAsync, a torch CUDA
+ *   tensor's data_ptr()), managed memory, or page-locked host memory mapped
+ *   into the unified address space (cudaHostAlloc, cudaHostRegister, a
+ *   pinned torch CPU tensor's data_ptr()): the kernels then read and write
+ *   host memory over the host link, with no staging copy.  Pageable host
+ *   memory returns OSR_ERR_INVALID.  The caller owns every buffer; the
+ *   library keeps no pointer after the call returns.
  * - Matrices are row-major and dense: row i starts at element i * (row
  *   length).  Rows of length H (norms) or N (softmax).
  * - Arithmetic is binary32 for every dtype (bfloat16 inputs are widened
@@ -195,8 +199,8 @@ osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t
  * OSR_ERR_UNSUPPORTED); a row must fit 16 CTAs' shared memory (192 KiB of
  * elements each: N <= 1.5 Mi bfloat16 or 786 Ki binary32) and N < 2^31,
  * else OSR_ERR_UNSUPPORTED.  Outputs must not overlap x or each other
- * (OSR_ERR_ALIAS).  All buffers are caller-owned device memory; the call is
- * asynchronous on `stream` and allocates nothing.
+ * (OSR_ERR_ALIAS).  All buffers are caller-owned (see the conventions);
+ * the call is asynchronous on `stream` and allocates nothing.
  */
 osr_status osr_row_topk(const void *x, float *values, int64_t *indices, float *probs, float *lse,
                         int64_t M, int64_t N, int64_t k, osr_dtype in_dt, void *stream);

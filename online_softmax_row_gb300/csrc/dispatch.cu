@@ -542,9 +542,11 @@ bool overlaps(const void *a, int64_t an, const void *b, int64_t bn) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// The buffer must be memory the device can address: device, managed, or
-// (on systems with unified addressing of host memory) registered-mapped host
-// memory is reported by the runtime; plain unregistered host memory is not.
+// The buffer must be memory the device can address at that same address:
+// device or managed memory, or page-locked host memory that the runtime maps
+// into the unified address space (cudaHostAlloc / cudaHostRegister on a
+// unified-addressing system: the kernels then read and write it over the
+// host link, no staging copy).  Pageable host memory is refused.
 bool device_accessible(const void *p) {
     cudaPointerAttributes at;
     cudaError_t e = cudaPointerGetAttributes(&at, p);
@@ -552,7 +554,8 @@ bool device_accessible(const void *p) {
         cudaGetLastError();
         return false;
     }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+    return at.type == cudaMemoryTypeHost && at.devicePointer == p;
 }
 
 osr_status check_sizes(int64_t M, int64_t N) {

@@ -314,3 +314,30 @@ def test_workload_full_size(name):
         out = osr.fused_add_rmsnorm(inp["x"].cuda(), res, inp["gamma"].cuda(), w.eps)
         check_fused(inp, out, res)
     torch.cuda.empty_cache()
+
+
+def test_pinned_host_buffers_zero_copy_and_pageable_refused():
+    # page-locked host buffers go straight to the kernels (read and written
+    # over the host link): the results are bit-identical to device buffers
+    import ctypes
+    lib = osr.library()
+    st = torch.cuda.current_stream().cuda_stream
+    inp = rms_case(64, 4096, "bf16", seed_of("host", 1), fused=True)
+    hx, hr, hg = (inp[k].clone().pin_memory() for k in ("x", "residual", "gamma"))
+    hy = torch.empty_like(hx).pin_memory()
+    assert lib.osr_fused_add_rmsnorm(hx.data_ptr(), hr.data_ptr(), hg.data_ptr(), ctypes.c_float(EPS),
+                                     hy.data_ptr(), 64, 4096, 1, st) == 0
+    torch.cuda.synchronize()
+    dr = inp["residual"].cuda()
+    dy = osr.fused_add_rmsnorm(inp["x"].cuda(), dr, inp["gamma"].cuda(), EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(hr, dr.cpu()) and torch.equal(hy, dy.cpu())
+    xs = sm_case(8, 152064, "bf16", seed_of("host", 2))["x"]
+    hx2 = xs.clone().pin_memory()
+    hy2 = torch.empty(8, 152064, dtype=torch.float32).pin_memory()
+    assert lib.osr_softmax_rows(hx2.data_ptr(), hy2.data_ptr(), 8, 152064, 1, 0, st) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(hy2, osr.softmax_rows(xs.cuda(), out_dtype=torch.float32).cpu())
+    # pageable host memory is refused before any launch
+    px, py = xs.clone(), torch.empty(8, 152064, dtype=torch.float32)
+    assert lib.osr_softmax_rows(px.data_ptr(), py.data_ptr(), 8, 152064, 1, 0, st) == 1
