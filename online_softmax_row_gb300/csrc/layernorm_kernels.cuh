@@ -80,6 +80,22 @@ layernorm_rows_kernel(const RowArgs a) {
         }
     }
     const uint64_t p2 = f2_make(p, p);
+    // binary32 vectors: the pivot-shifted pairs are formed once and kept (the
+    // same registers as the raw vectors; 4.30 -> 4.13 us on 256 x 5120).
+    // bfloat16 vectors stay packed and are widened in each pass: keeping the
+    // wide pairs costs 52 instead of 38 registers and measured 2 % slower.
+    constexpr bool kKeep = kVec && D == Dt::F32;
+    uint64_t d2[kKeep ? NU : 1][kKeep ? PAIRS : 1];
+    if constexpr (kKeep) {
+#pragma unroll
+        for (int j = 0; j < NU; ++j)
+#pragma unroll
+            for (int k = 0; k < PAIRS; ++k) d2[j][k] = f2_sub(f2_of<D>(q[j], k), p2);
+    }
+    auto shifted2 = [&](int j, int k) {  // pair k of unit j, minus the pivot
+        if constexpr (kKeep) return d2[j][k];
+        else return f2_sub(f2_of<D>(q[j], k), p2);
+    };
 
     // sum of the pivot-shifted values
     float s1 = 0.f;
@@ -89,7 +105,7 @@ layernorm_rows_kernel(const RowArgs a) {
         for (int j = 0; j < NU; ++j)
             if (valid >> j & 1u) {
 #pragma unroll
-                for (int k = 0; k < PAIRS; ++k) acc = f2_add(acc, f2_sub(f2_of<D>(q[j], k), p2));
+                for (int k = 0; k < PAIRS; ++k) acc = f2_add(acc, shifted2(j, k));
             }
         s1 = f2_lo(acc) + f2_hi(acc);
     } else {
@@ -117,7 +133,7 @@ layernorm_rows_kernel(const RowArgs a) {
             if (valid >> j & 1u) {
 #pragma unroll
                 for (int k = 0; k < PAIRS; ++k) {
-                    const uint64_t c = f2_sub(f2_sub(f2_of<D>(q[j], k), p2), mu2);
+                    const uint64_t c = f2_sub(shifted2(j, k), mu2);
                     acc = f2_fma(c, c, acc);
                 }
             }
@@ -156,7 +172,7 @@ layernorm_rows_kernel(const RowArgs a) {
             uint64_t o[PAIRS];
 #pragma unroll
             for (int k = 0; k < PAIRS; ++k) {
-                const uint64_t z = f2_mul(f2_sub(f2_sub(f2_of<D>(q[j], k), p2), mu2), r2);
+                const uint64_t z = f2_mul(f2_sub(shifted2(j, k), mu2), r2);
                 o[k] = f2_fma(z, f2_of<D>(g16, k), f2_of<D>(b16, k));
             }
             uint4 w;
