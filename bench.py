@@ -530,7 +530,9 @@ def ours(args):
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.in_dtype == "bf16" else "f32", "data": "synthetic",
+        # the arithmetic type: every kernel computes in binary32 (bf16 inputs
+        # are widened exactly); the storage types are in_dtype / out_dtype
+        "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
                    "out_dtype": w.out_dtype, "min_bytes_per_step": w.min_bytes, "kernel": plan,
                    "rows_capped": bool(args.max_rows and w.M == args.max_rows),
