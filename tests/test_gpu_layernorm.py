@@ -146,3 +146,18 @@ def test_layernorm_workloads_full_size():
         y = osr.layernorm_fwd(inp["x"].cuda(), inp["gamma"].cuda(), inp["beta"].cuda(), w.eps)
         torch.cuda.synchronize()
         check_ln(inp["x"], inp["gamma"], inp["beta"], y)
+
+
+def test_layernorm_on_pinned_host_rows():
+    import ctypes
+    lib = osr.library()
+    inp = workloads.layernorm_inputs(16, 5120, "f32", low=100.0, high=102.0, seed=31)
+    hx, hg, hb = (inp[k].clone().pin_memory() for k in ("x", "gamma", "beta"))
+    hy = torch.empty_like(hx).pin_memory()
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.osr_layernorm_fwd(hx.data_ptr(), hg.data_ptr(), hb.data_ptr(), ctypes.c_float(1e-5),
+                                 hy.data_ptr(), 16, 5120, 0, st) == 0
+    torch.cuda.synchronize()
+    dy = osr.layernorm_fwd(inp["x"].cuda(), inp["gamma"].cuda(), inp["beta"].cuda(), 1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(hy, dy.cpu())

@@ -171,3 +171,24 @@ def test_topk_constant_rows(spec):
     torch.cuda.synchronize()
     check(x, 50, *out, what=f"constant {spec or 'default'}")
     assert out[1].cpu().tolist() == [list(range(50))] * 3
+
+
+def test_topk_on_pinned_host_rows():
+    # page-locked host rows go straight to the kernel (cp.async from host
+    # memory over the host link): the same result as device rows
+    import ctypes
+    lib = osr.library()
+    x = rows(4, 152064, "bf16", seed=21)
+    hx = x.clone().pin_memory()
+    hv = torch.empty(4, 50, dtype=torch.float32).pin_memory()
+    hi = torch.empty(4, 50, dtype=torch.int64).pin_memory()
+    hp = torch.empty(4, 50, dtype=torch.float32).pin_memory()
+    hl = torch.empty(4, dtype=torch.float32).pin_memory()
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.osr_row_topk(hx.data_ptr(), hv.data_ptr(), hi.data_ptr(), hp.data_ptr(), hl.data_ptr(),
+                            4, 152064, 50, 1, st) == 0
+    torch.cuda.synchronize()
+    dv, di, dp, dl = osr.row_topk(x.cuda(), 50)
+    torch.cuda.synchronize()
+    assert torch.equal(hi, di.cpu()) and torch.equal(hv, dv.cpu())
+    assert torch.equal(hp, dp.cpu()) and torch.equal(hl, dl.cpu())
