@@ -20,6 +20,7 @@
 
 #include "../../include/osr.h"
 #include "launch.h"
+#include "staged.h"
 #include "topk.h"
 
 namespace osr {
@@ -110,21 +111,47 @@ int64_t pow2_at_least(int64_t v) {
     return c;
 }
 
-// Staged tier shape.  Few rows (three CTAs per SM would need 8 or more per
+// Whether the staged tier holds part of each piece in registers by default.
+bool staged_regs(osr_dtype in_dt, osr_dtype out_dt) { return !(in_dt == OSR_BF16 && out_dt == OSR_F32); }
+
+// Staged tier shape.
+//
+// regs (the default except for bfloat16 in, fp32 out): each thread holds
+// kStagedRegUnits units in registers and the rest of its piece is staged.
+// The fewest pieces of at most 76 KiB (about half in registers, so four CTAs
+// fit an SM); with fewer CTAs than SMs, 12 pieces (16 for one or two rows).
+// Measured against the shared-memory-only shapes below on fp32 rows of
+// 24 Ki to 256 Ki elements and bfloat16 rows of 20 Ki to 148 Ki: 0-26 %
+// faster (441 x 152064 fp32: 96.2 -> 87.6 us; 2048 x 32768 bf16: 52.6 ->
+// 48.9 us); bfloat16 -> fp32 rows ran 2-15 % slower with registers.
+//
+// Without registers: few rows (three CTAs per SM would need 8 or more per
 // row): 12 CTAs per row, 16 for one or two rows.  Otherwise the fewest CTAs
 // whose pieces fit 96 KiB (or, failing that, 200 KiB), raised toward three
 // CTAs per SM, at least 8 for rows of 192 KiB or more, and rounded up to a
 // power of two, which packs the GPCs better (measured: 152064-element rows
-// ran 13 % faster as 8 pieces than as 7).  force_cs: 0 decide.  Returns
-// false if no piece within the limits holds the row.
-bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, int64_t force_cs, Plan *p) {
+// ran 13 % faster as 8 pieces than as 7).
+//
+// force_cs: 0 decide; force_ru: -1 decide.  Returns false if no piece within
+// the limits holds the row.
+bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, bool regs,
+                  int64_t force_cs, int64_t force_ru, int64_t force_g, Plan *p) {
     const int64_t row_bytes = nunits * 16;
+    const int64_t ru = force_ru >= 0 ? force_ru : regs ? kStagedRegUnits : 0;
+    const int64_t threads = force_g > 0 ? force_g : ru > 0 ? kStagedRegThreads : kStagedThreads;
+    if (threads > 1024 || !staged_shape_ok((int)threads, (int)ru)) return false;
+    const int64_t most = cdiv(nunits, threads);  // >= one unit per thread
     int64_t cs = force_cs;
-    if (cs <= 0) {
+    if (cs <= 0 && ru > 0) {
+        cs = cdiv(row_bytes, kStagedRegPieceBytes);
+        const int64_t wide = M <= 2 ? 16 : 12;
+        if (M * cs < sms && cs < wide) cs = wide;
+        if (cs > max_cluster) cs = max_cluster;
+        if (cs > most) cs = most;
+    } else if (cs <= 0) {
         int64_t need = cdiv(row_bytes, kStagedPreferBytes);
         if (need > max_cluster) need = cdiv(row_bytes, kStagedMaxSmem - 128);
         int64_t fill = cdiv(3 * (int64_t)sms, M);
-        const int64_t most = cdiv(nunits, kStagedThreads);  // >= one unit per thread
         if (fill >= 8 && need <= 12) {
             // few rows: spread each row wide.  Measured on 1..64 rows of 64 Ki
             // to 152 Ki elements: 16 CTAs for one or two rows, 12 otherwise
@@ -146,13 +173,15 @@ bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, int64_t f
     }
     if (cs < 1 || cs > max_cluster) return false;
     const int64_t chunk = cdiv(nunits, cs);
-    const int64_t smem = 128 + chunk * 16;
+    const int64_t held = threads * ru;  // units a CTA holds in registers
+    const int64_t smem = 128 + (chunk > held ? chunk - held : 0) * 16;
     if (smem > kStagedMaxSmem) return false;
     p->tier = Tier::Staged;
-    p->g = kStagedThreads;
+    p->g = (int)threads;
     p->cs = (int)cs;
     p->chunk = chunk;
     p->smem = (size_t)smem;
+    p->ru = (int)ru;
     return true;
 }
 
@@ -182,7 +211,6 @@ void split_shape(Op op, int64_t M, int64_t N, int64_t nunits, int in_bytes, int 
 
 osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt, bool vec,
                      int sms, int max_cluster, Plan *p) {
-    (void)out_dt;
     *p = Plan();
     p->vec = vec;
     p->u = vec ? vec_elems(in_dt) : 1;
@@ -216,9 +244,14 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
         }
         if (strncmp(force, "staged", 6) == 0) {
             if (op != Op::Softmax || !vec) return OSR_ERR_UNSUPPORTED;
+            int64_t ru = -1;
             parse_kv(force, "cs", &cs);
+            parse_kv(force, "r", &ru);
+            parse_kv(force, "g", &g);
             if (cs <= 0) cs = 0;
-            return staged_shape(M, nunits, sms, max_cluster, cs, p) ? OSR_OK : OSR_ERR_UNSUPPORTED;
+            return staged_shape(M, nunits, sms, max_cluster, staged_regs(in_dt, out_dt), cs, ru, g, p)
+                       ? OSR_OK
+                       : OSR_ERR_UNSUPPORTED;
         }
         if (strncmp(force, "split", 5) == 0) {
             parse_kv(force, "s", &s);
@@ -243,7 +276,9 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
     }
     // 2. softmax on 16-byte rows: a cluster per row, pieces staged in shared
     //    memory by bulk copies (one read)
-    if (op == Op::Softmax && vec && staged_shape(M, nunits, sms, max_cluster, 0, p)) return OSR_OK;
+    if (op == Op::Softmax && vec &&
+        staged_shape(M, nunits, sms, max_cluster, staged_regs(in_dt, out_dt), 0, -1, 0, p))
+        return OSR_OK;
     // 3. a cluster of 1024-thread CTAs, still register-cached (one read)
     const int64_t cs = cdiv(nunits, (int64_t)1024 * upt);
     if (cs <= max_cluster) {
@@ -316,7 +351,11 @@ void describe(const Plan &p, char *buf, size_t n) {
                  p.ept, v);
         break;
     case Tier::Staged:
-        snprintf(buf, n, "staged cs=%d g=%d piece=%lldB %s", p.cs, p.g, (long long)p.chunk * 16, v);
+        if (p.ru)
+            snprintf(buf, n, "staged cs=%d g=%d piece=%lldB r=%d %s", p.cs, p.g, (long long)p.chunk * 16,
+                     p.ru, v);
+        else
+            snprintf(buf, n, "staged cs=%d g=%d piece=%lldB %s", p.cs, p.g, (long long)p.chunk * 16, v);
         break;
     }
 }
@@ -371,24 +410,24 @@ cudaError_t cluster_occupancy(Op op, osr_dtype in_dt, osr_dtype out_dt, const Pl
 // occupancy query are cached per device and kernel shape.
 cudaError_t staged_occupancy(osr_dtype in_dt, osr_dtype out_dt, const Plan &p, int *n) {
     if (in_dt == OSR_F32 && out_dt == OSR_F32)
-        return softmax_staged_occupancy<Dt::F32, Dt::F32>(p.cs, p.smem, n);
+        return softmax_staged_occupancy<Dt::F32, Dt::F32>(p.cs, p.smem, p.g, p.ru, n);
     if (in_dt == OSR_F32 && out_dt == OSR_BF16)
-        return softmax_staged_occupancy<Dt::F32, Dt::BF16>(p.cs, p.smem, n);
+        return softmax_staged_occupancy<Dt::F32, Dt::BF16>(p.cs, p.smem, p.g, p.ru, n);
     if (in_dt == OSR_BF16 && out_dt == OSR_F32)
-        return softmax_staged_occupancy<Dt::BF16, Dt::F32>(p.cs, p.smem, n);
-    return softmax_staged_occupancy<Dt::BF16, Dt::BF16>(p.cs, p.smem, n);
+        return softmax_staged_occupancy<Dt::BF16, Dt::F32>(p.cs, p.smem, p.g, p.ru, n);
+    return softmax_staged_occupancy<Dt::BF16, Dt::BF16>(p.cs, p.smem, p.g, p.ru, n);
 }
 
 osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                               const DeviceInfo &di, Plan *p) {
     if (p->tier != Tier::Cluster && p->tier != Tier::Staged) return OSR_OK;
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, int, int, int, int, size_t>, int> cache;
+    static std::map<std::tuple<int, int, int, int, int, int, int, int, size_t, int>, int> cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     const auto key = std::make_tuple(dev, (int)op, (int)in_dt, (int)out_dt, (int)p->tier, p->g,
-                                     (int)p->vec, p->cs, p->smem);
+                                     (int)p->vec, p->cs, p->smem, p->ru);
     int n = -1;
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -495,13 +534,13 @@ osr_status execute(Op op, osr_dtype in_dt, osr_dtype out_dt, RowArgs a, const Pl
         const char *hook = getenv("OSR_TEST_HOOK");
         if (hook && strcmp(hook, "no_arrive") == 0) a.flags |= kFlagNoArrive;
         if (in_dt == OSR_F32 && out_dt == OSR_F32)
-            e = launch_softmax_staged<Dt::F32, Dt::F32>(a, grid, p.smem, st);
+            e = launch_softmax_staged<Dt::F32, Dt::F32>(a, grid, p.smem, p.g, p.ru, st);
         else if (in_dt == OSR_F32 && out_dt == OSR_BF16)
-            e = launch_softmax_staged<Dt::F32, Dt::BF16>(a, grid, p.smem, st);
+            e = launch_softmax_staged<Dt::F32, Dt::BF16>(a, grid, p.smem, p.g, p.ru, st);
         else if (in_dt == OSR_BF16 && out_dt == OSR_F32)
-            e = launch_softmax_staged<Dt::BF16, Dt::F32>(a, grid, p.smem, st);
+            e = launch_softmax_staged<Dt::BF16, Dt::F32>(a, grid, p.smem, p.g, p.ru, st);
         else
-            e = launch_softmax_staged<Dt::BF16, Dt::BF16>(a, grid, p.smem, st);
+            e = launch_softmax_staged<Dt::BF16, Dt::BF16>(a, grid, p.smem, p.g, p.ru, st);
         break;
     }
     case Tier::Split: {

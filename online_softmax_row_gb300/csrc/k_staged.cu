@@ -24,6 +24,7 @@
 
 #include "../../include/osr.h"
 #include "launch.h"
+#include "staged.h"
 
 namespace osr {
 
@@ -34,8 +35,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000; // 1 s
 static __device__ unsigned int g_staged_fault;
 
 template <Dt D>
-__device__ __forceinline__ void lds_unit(const unsigned char *p, float (&v)[Elem<D>::kVec]) {
-    const uint4 q = *reinterpret_cast<const uint4 *>(p);
+__device__ __forceinline__ void unit_values(const uint4 &q, float (&v)[Elem<D>::kVec]) {
     if constexpr (D == Dt::F32) {
         v[0] = __uint_as_float(q.x);
         v[1] = __uint_as_float(q.y);
@@ -45,11 +45,19 @@ __device__ __forceinline__ void lds_unit(const unsigned char *p, float (&v)[Elem
         unpack8(q, v);
     }
 }
+template <Dt D>
+__device__ __forceinline__ void lds_unit(const unsigned char *p, float (&v)[Elem<D>::kVec]) {
+    unit_values<D>(*reinterpret_cast<const uint4 *>(p), v);
+}
 
-template <Dt DI, Dt DO>
-__global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const RowArgs a) {
+// RU > 0: the first RU * T units of a piece are held in registers (RU raw
+// 16-byte vectors a thread, loaded with ordinary streaming loads while the
+// bulk copy of the rest is in flight); only the remainder is staged in shared
+// memory.  A CTA then holds about twice the bytes per unit of shared memory,
+// and with 64 registers a thread four 256-thread CTAs fit one SM.
+template <Dt DI, Dt DO, int T, int RU>
+__global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(const RowArgs a) {
     constexpr int U = Elem<DI>::kVec;
-    constexpr int T = kStagedThreads;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t bar = smem_u32(smem);
     const unsigned char *stage = smem + kStagedHeader;
@@ -59,6 +67,8 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
     const int64_t u0 = (int64_t)cluster_ctarank() * a.chunk;
     const int64_t u1 = u0 + a.chunk < nunits ? u0 + a.chunk : nunits;
     const int n = u1 > u0 ? (int)(u1 - u0) : 0;  // 16-byte units in this CTA's piece
+    const int nr = n < RU * T ? n : RU * T;       // of which held in registers
+    const int ns = n - nr;                        // and staged in shared memory
     const char *src = reinterpret_cast<const char *>(a.x) + (row * nunits + u0) * 16;
 
     if (threadIdx.x == 0) {
@@ -72,13 +82,26 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
         // the input is read exactly once: fetch it under an evict-first L2
         // policy (measured about 1 % faster than the default policy)
         const uint64_t policy = l2_evict_first_policy();
-        const uint32_t bytes = (uint32_t)n * 16u;
+        const uint32_t bytes = (uint32_t)ns * 16u;
         mbar_arrive_expect_tx(bar, bytes);
         for (uint32_t off = 0; off < bytes; off += kBulkPiece) {
             const uint32_t len = bytes - off < kBulkPiece ? bytes - off : kBulkPiece;
-            bulk_load_g2s_hint(smem_u32(stage) + off, src + off, len, bar, policy);
+            bulk_load_g2s_hint(smem_u32(stage) + off, src + (size_t)nr * 16 + off, len, bar, policy);
         }
     }
+    uint4 r[RU > 0 ? RU : 1];
+    float mt = -FLT_MAX, dt = 0.f;
+#pragma unroll
+    for (int j = 0; j < RU; ++j)
+        if (threadIdx.x + j * T < nr) r[j] = ld16<Hint::Stream>(src + (size_t)(threadIdx.x + j * T) * 16);
+#pragma unroll
+    for (int j = 0; j < RU; ++j)
+        if (threadIdx.x + j * T < nr) {
+            float v[U];
+            unit_values<DI>(r[j], v);
+#pragma unroll
+            for (int k = 0; k < U; ++k) mt = fmaxf(mt, v[k]);
+        }
     bool ok = mbar_wait_bounded(bar, 0, kWaitLimitNs);
     ok = __syncthreads_and(ok);
     if (!ok) {
@@ -87,20 +110,30 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
     }
 
     // this CTA's (m, d): its maximum, then its sum of exp(x - max)
-    float mt = -FLT_MAX, dt = 0.f;
     if (ok) {
-        for (int u = threadIdx.x; u < n; u += T) {
+        for (int u = threadIdx.x; u < ns; u += T) {
             float v[U];
             lds_unit<DI>(stage + u * 16, v);
 #pragma unroll
             for (int k = 0; k < U; ++k) mt = fmaxf(mt, v[k]);
         }
-        for (int u = threadIdx.x; u < n; u += T) {
+#pragma unroll
+        for (int j = 0; j < RU; ++j)
+            if (threadIdx.x + j * T < nr) {
+                float v[U];
+                unit_values<DI>(r[j], v);
+#pragma unroll
+                for (int k = 0; k < U; ++k) dt += exp_shifted(v[k], mt);
+            }
+        for (int u = threadIdx.x; u < ns; u += T) {
             float v[U];
             lds_unit<DI>(stage + u * 16, v);
 #pragma unroll
             for (int k = 0; k < U; ++k) dt += exp_shifted(v[k], mt);
         }
+    } else {
+        mt = -FLT_MAX;
+        dt = 0.f;
     }
     __shared__ float red_m[32], red_d[32];
     __shared__ float2 slot;
@@ -115,13 +148,23 @@ __global__ void __launch_bounds__(kStagedThreads) softmax_staged_kernel(const Ro
         const float inv_d = 1.0f / rn.d, logd = logf(rn.d);
         const bool logm = (a.flags & kFlagLog) != 0;
         char *yrow = reinterpret_cast<char *>(a.y) + row * a.N * Elem<DO>::kBytes;
-        for (int u = threadIdx.x; u < n; u += T) {
+#pragma unroll
+        for (int j = 0; j < RU; ++j)
+            if (threadIdx.x + j * T < nr) {
+                float v[U], o[U];
+                unit_values<DI>(r[j], v);
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    o[k] = logm ? (v[k] - rn.m) - logd : exp_shifted(v[k], rn.m) * inv_d;
+                store_unit<DO, U>(yrow, (u0 + threadIdx.x + j * T) * U, o);
+            }
+        for (int u = threadIdx.x; u < ns; u += T) {
             float v[U], o[U];
             lds_unit<DI>(stage + u * 16, v);
 #pragma unroll
             for (int k = 0; k < U; ++k)
                 o[k] = logm ? (v[k] - rn.m) - logd : exp_shifted(v[k], rn.m) * inv_d;
-            store_unit<DO, U>(yrow, (u0 + u) * U, o);
+            store_unit<DO, U>(yrow, (u0 + nr + u) * U, o);
         }
     }
     pdl_trigger();
@@ -132,7 +175,7 @@ namespace {
 
 // Per-device, per-kernel one-time attribute setup (dynamic shared memory
 // above 48 KiB, cluster sizes above 8).
-template <Dt DI, Dt DO>
+template <Dt DI, Dt DO, int T, int RU>
 cudaError_t prepare() {
     static std::mutex mu;
     static bool done[64] = {};
@@ -142,7 +185,7 @@ cudaError_t prepare() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
-        auto k = softmax_staged_kernel<DI, DO>;
+        auto k = softmax_staged_kernel<DI, DO, T, RU>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedMaxSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -152,11 +195,11 @@ cudaError_t prepare() {
     return cudaSuccess;
 }
 
-cudaLaunchConfig_t staged_config(int64_t grid, size_t smem, int cs, cudaStream_t st,
+cudaLaunchConfig_t staged_config(int64_t grid, int threads, size_t smem, int cs, cudaStream_t st,
                                  cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kStagedThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -170,31 +213,50 @@ cudaLaunchConfig_t staged_config(int64_t grid, size_t smem, int cs, cudaStream_t
     return cfg;
 }
 
+template <Dt DI, Dt DO, int T, int RU>
+cudaError_t launch_shape(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st) {
+    cudaError_t e = prepare<DI, DO, T, RU>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = staged_config(grid, T, smem, a.cs, st, attr);
+    return cudaLaunchKernelEx(&cfg, softmax_staged_kernel<DI, DO, T, RU>, a);
+}
+
+template <Dt DI, Dt DO, int T, int RU>
+cudaError_t occupancy_shape(int cs, size_t smem, int *n) {
+    cudaError_t e = prepare<DI, DO, T, RU>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = staged_config((int64_t)cs * 64, T, smem, cs, nullptr, attr);
+    return cudaOccupancyMaxActiveClusters(n, softmax_staged_kernel<DI, DO, T, RU>, &cfg);
+}
+
 }  // namespace
 
 template <Dt DI, Dt DO>
-cudaError_t launch_softmax_staged(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st) {
-    cudaError_t e = prepare<DI, DO>();
-    if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = staged_config(grid, smem, a.cs, st, attr);
-    return cudaLaunchKernelEx(&cfg, softmax_staged_kernel<DI, DO>, a);
+cudaError_t launch_softmax_staged(const RowArgs &a, int64_t grid, size_t smem, int threads, int ru,
+                                  cudaStream_t st) {
+    if (threads == kStagedThreads && ru == 0)
+        return launch_shape<DI, DO, kStagedThreads, 0>(a, grid, smem, st);
+    if (threads == kStagedRegThreads && ru == kStagedRegUnits)
+        return launch_shape<DI, DO, kStagedRegThreads, kStagedRegUnits>(a, grid, smem, st);
+    return cudaErrorInvalidValue;
 }
 
 template <Dt DI, Dt DO>
-cudaError_t softmax_staged_occupancy(int cs, size_t smem, int *n) {
+cudaError_t softmax_staged_occupancy(int cs, size_t smem, int threads, int ru, int *n) {
     *n = 0;
-    cudaError_t e = prepare<DI, DO>();
-    if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = staged_config((int64_t)cs * 64, smem, cs, nullptr, attr);
-    return cudaOccupancyMaxActiveClusters(n, softmax_staged_kernel<DI, DO>, &cfg);
+    if (threads == kStagedThreads && ru == 0)
+        return occupancy_shape<DI, DO, kStagedThreads, 0>(cs, smem, n);
+    if (threads == kStagedRegThreads && ru == kStagedRegUnits)
+        return occupancy_shape<DI, DO, kStagedRegThreads, kStagedRegUnits>(cs, smem, n);
+    return cudaErrorInvalidValue;
 }
 
-#define OSR_STAGED(DI, DO)                                                                    \
+#define OSR_STAGED(DI, DO)                                                                      \
     template cudaError_t launch_softmax_staged<Dt::DI, Dt::DO>(const RowArgs &, int64_t, size_t, \
-                                                               cudaStream_t);                 \
-    template cudaError_t softmax_staged_occupancy<Dt::DI, Dt::DO>(int, size_t, int *);
+                                                               int, int, cudaStream_t);         \
+    template cudaError_t softmax_staged_occupancy<Dt::DI, Dt::DO>(int, size_t, int, int, int *);
 OSR_STAGED(F32, F32)
 OSR_STAGED(F32, BF16)
 OSR_STAGED(BF16, F32)

@@ -41,9 +41,6 @@ constexpr int softmax_ept() {
 }
 constexpr int kSplitThreads = 512;  // threads per split-row CTA
 constexpr int kMaxPieces = kSplitThreads;
-constexpr int kStagedThreads = 256;               // threads per staged CTA
-constexpr int kStagedPreferBytes = 96 << 10;      // piece size that leaves room for 2 CTAs/SM
-constexpr int kStagedMaxSmem = 200 << 10;         // largest staged piece + header
 
 // Launch with programmatic dependent launch (default on; OSR_PDL=0 turns it
 // off).  Read once per process.
@@ -65,6 +62,7 @@ struct Plan {
     bool vec = true;         // 16-byte units (true) or element units
     int u = 1;               // elements per unit
     int ept = kEpt;          // elements per thread per tile
+    int ru = 0;              // Staged: 16-byte units a thread holds in registers
     bool forced = false;
 };
 
@@ -96,12 +94,5 @@ cudaError_t rmsnorm_cluster_occupancy(int g, bool vec, int cs, int *n);
 template <Dt DI>
 cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t grid,
                        cudaStream_t st);
-
-// Staged softmax tier (k_staged.cu): grid = rows * a.cs CTAs of
-// kStagedThreads, clusters of a.cs, `smem` bytes of dynamic shared memory.
-template <Dt DI, Dt DO>
-cudaError_t launch_softmax_staged(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st);
-template <Dt DI, Dt DO>
-cudaError_t softmax_staged_occupancy(int cs, size_t smem, int *n);
 
 }  // namespace osr

@@ -101,23 +101,42 @@ def test_bench_copy_validation(lib):
 @pytest.mark.parametrize("n,tier", [
     (1, "rows g=1"), (32, "rows g=2"), (128, "rows g=8"), (1024, "rows g=64"),
     (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "staged cs=12"),
-    (152064, "staged cs=12"), (262144, "staged cs=12"), (1 << 20, "split"),
+    (152064, "staged cs=8"), (262144, "staged cs=14"), (1 << 20, "split"),
 ])
 def test_dispatch_tiers_softmax_f32(lib, n, tier):
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, n, "f32").startswith(tier)
 
 
 @pytest.mark.parametrize("m,n,want", [
-    (2048, 32768, "staged cs=2 g=256 piece=65536B"),     # 2 pieces of 64 KiB
-    (441, 152064, "staged cs=8 g=256 piece=76032B"),     # fewest pieces <= 96 KiB, 2^k
-    (128, 65536, "staged cs=8 g=256 piece=32768B"),      # rows >= 192 KiB: at least 8
-    (64, 152064, "staged cs=12 g=256 piece=50688B"),     # few rows: spread over 12 CTAs
-    (8, 65536, "staged cs=12 g=256 piece=21856B"),
-    (1, 32768, "staged cs=16 g=256 piece=8192B"),        # one row: spread over 16 CTAs
-    (3, 800000, "staged cs=16 g=256 piece=200000B"),     # largest pieces
+    # part of each piece in registers: the fewest pieces of at most 76 KiB
+    (2048, 32768, "staged cs=2 g=256 piece=65536B r=8 vec"),
+    (441, 152064, "staged cs=8 g=256 piece=76032B r=8 vec"),
+    (128, 65536, "staged cs=4 g=256 piece=65536B r=8 vec"),
+    (256, 98304, "staged cs=6 g=256 piece=65536B r=8 vec"),
+    (2048, 40960, "staged cs=3 g=256 piece=54624B r=8 vec"),     # ragged: 3414 + 3414 + 3412 units
+    (64, 152064, "staged cs=8 g=256 piece=76032B r=8 vec"),
+    # fewer CTAs than SMs: spread over 12 CTAs, 16 for one or two rows
+    (16, 152064, "staged cs=12 g=256 piece=50688B r=8 vec"),
+    (8, 65536, "staged cs=12 g=256 piece=21856B r=8 vec"),
+    (1, 32768, "staged cs=16 g=256 piece=8192B r=8 vec"),
+    (3, 800000, "staged cs=16 g=256 piece=200000B r=8 vec"),    # largest pieces
 ])
 def test_dispatch_staged_shapes(m, n, want):
-    assert osr.plan_describe(osr.OP_SOFTMAX, m, n, "f32").startswith(want)
+    assert osr.plan_describe(osr.OP_SOFTMAX, m, n, "f32") == want
+
+
+@pytest.mark.parametrize("m,n,io,want", [
+    # bfloat16 -> fp32 rows stage whole pieces in shared memory
+    (441, 152064, ("bf16", "f32"), "staged cs=8 g=256 piece=38016B vec"),     # pieces <= 96 KiB, 2^k
+    (64, 152064, ("bf16", "f32"), "staged cs=12 g=256 piece=25344B vec"),     # few rows: 12 CTAs
+    (2048, 32768, ("bf16", "f32"), "staged cs=1 g=256 piece=65536B vec"),
+    # bfloat16 -> bfloat16 and fp32 -> bfloat16 hold part in registers
+    (2048, 32768, ("bf16", "bf16"), "staged cs=1 g=256 piece=65536B r=8 vec"),
+    (512, 152064, ("bf16", "bf16"), "staged cs=4 g=256 piece=76032B r=8 vec"),
+    (441, 152064, ("f32", "bf16"), "staged cs=8 g=256 piece=76032B r=8 vec"),
+])
+def test_dispatch_staged_shapes_by_dtype(m, n, io, want):
+    assert osr.plan_describe(osr.OP_SOFTMAX, m, n, *io) == want
 
 
 def test_dispatch_long_rows_without_staging():
@@ -178,6 +197,14 @@ def test_forced_kernel(monkeypatch):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
     monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3")
     assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("staged cs=3 g=256 piece=6672B")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3,r=8")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32") == "staged cs=3 g=256 piece=6672B r=8 vec"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3,g=128,r=8")  # only the compiled shapes
+    with pytest.raises(osr.OsrError):
+        osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3,r=5")
+    with pytest.raises(osr.OsrError):
+        osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
     for bad in ((osr.OP_RMSNORM, True), (osr.OP_SOFTMAX, False)):  # softmax, 16-byte rows only
         with pytest.raises(osr.OsrError):
             osr.plan_describe(bad[0], 10, 5000, "f32", vec_ok=bad[1])

@@ -139,7 +139,8 @@ def test_forced_tiers(spec, dt):
 
 
 @pytest.mark.parametrize("spec", ["staged:cs=1", "staged:cs=2", "staged:cs=5", "staged:cs=16",
-                                  "staged:cs=3", "staged:cs=8"])
+                                  "staged:cs=3", "staged:cs=8", "staged:cs=1,r=0", "staged:cs=3,r=0",
+                                  "staged:cs=16,r=0"])
 @pytest.mark.parametrize("io", [("f32", "f32"), ("bf16", "f32"), ("f32", "bf16"), ("bf16", "bf16")])
 def test_forced_staged(spec, io):
     M, N = 37, 5000
@@ -149,7 +150,23 @@ def test_forced_staged(spec, io):
     check_softmax(inp, y, rmax, rsum)
 
 
-@pytest.mark.parametrize("spec", ["cluster:g=1024,cs=16", "split:s=512,b=1", "staged:cs=16"])
+# part of each piece held in registers: 5000-element rows fit the registers
+# whole (no bulk copy at all); 40008-element rows leave a staged remainder,
+# ragged over 3 pieces
+@pytest.mark.parametrize("spec", ["staged:cs=1,r=8", "staged:cs=3,r=8", "staged:cs=2,r=8",
+                                  "staged:cs=1,r=0", "staged:cs=3,r=0"])
+@pytest.mark.parametrize("N", [5000, 40008])
+@pytest.mark.parametrize("io", [("f32", "f32"), ("bf16", "f32"), ("f32", "bf16"), ("bf16", "bf16")])
+def test_forced_staged_registers(spec, N, io):
+    M = 5
+    inp = sm_case(M, N, io[0], seed_of("staged-r", spec, N, io))
+    y, rmax, rsum = run_forced(spec, lambda: osr.softmax_rows_stats(inp["x"].cuda(),
+                                                                    out_dtype=DT[io[1]]))
+    check_softmax(inp, y, rmax, rsum)
+
+
+@pytest.mark.parametrize("spec", ["cluster:g=1024,cs=16", "split:s=512,b=1", "staged:cs=16,r=0",
+                                  "staged:cs=16,r=8"])
 def test_forced_limits(spec):
     M, N = 3, 200000
     inp = sm_case(M, N, "f32", seed_of("limits", spec))
