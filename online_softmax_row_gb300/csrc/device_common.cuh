@@ -270,6 +270,15 @@ __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
     return v;
 }
 
+// Asynchronous store of two floats into shared memory of a CTA of the
+// cluster (addresses from mapa_shared), completing `8` bytes on that CTA's
+// mbarrier, which the receiver waits on: no cluster barrier orders it.
+__device__ __forceinline__ void st_async_f2(uint32_t addr, uint32_t remote_bar, float x, float y) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(x), "f"(y), "r"(remote_bar)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copies
 // 1-D bulk asynchronous copies (the TMA engine, no tensor map) from global
 // into this CTA's shared memory, completed through an mbarrier's

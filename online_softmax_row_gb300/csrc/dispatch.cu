@@ -171,7 +171,7 @@ bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, bool regs
             if (c2 <= max_cluster && cdiv(nunits, c2) >= kStagedThreads / 4) cs = c2;
         }
     }
-    if (cs < 1 || cs > max_cluster) return false;
+    if (cs < 1 || cs > max_cluster || cs > kStagedMaxCluster) return false;
     const int64_t chunk = cdiv(nunits, cs);
     const int64_t held = threads * ru;  // units a CTA holds in registers
     const int64_t smem = 128 + (chunk > held ? chunk - held : 0) * 16;

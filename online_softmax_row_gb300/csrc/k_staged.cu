@@ -2,22 +2,28 @@
 // CTA's registers hold (16-byte aligned rows).
 //
 // A row is cut into cs pieces, one per CTA of a thread-block cluster.  Each
-// CTA pulls its whole piece from HBM into shared memory with 1-D bulk
-// asynchronous copies (the TMA engine) completing on one mbarrier, so a
-// CTA of 256 threads keeps tens of KiB in flight without spending registers
-// on them.  From shared memory the CTA takes its maximum and its sum of
-// exp(x - max), the cs partial (m, d) states are exchanged through
-// distributed shared memory and reduced max-then-sum, and every CTA writes
-// its piece of y = exp(x - m) / d.  One HBM read and one HBM write per
-// element, as in "两个融合算子：RMSNorm 与 online softmax" §4 (the row stays
-// on chip) -- here on chip means shared memory spread over a cluster, which
-// is how rows far beyond that page's 8192-element limit (§4·五) stay
-// single-pass.
+// CTA pulls its piece from HBM with 1-D bulk asynchronous copies (the TMA
+// engine) into shared memory, completing on one mbarrier -- or, with RU > 0,
+// holds the first part of it in registers and bulk-copies only the rest.
+// The CTA takes its maximum and its sum of exp(x - max), stores this (m, d)
+// into every CTA of the cluster with st.async (distributed shared memory,
+// counted on the receiver's own mbarrier), reduces the cs states
+// max-then-sum in a fixed order, and writes its piece of y = exp(x - m) / d.
+// One HBM read and one HBM write per element, as in "两个融合算子：RMSNorm 与
+// online softmax" §4 (the row stays on chip) -- here on chip means the
+// registers and shared memory of a cluster, which is how rows far beyond
+// that page's 8192-element limit (§4·五) stay single-pass.
 //
-// The only wait on the copies is bounded (1 s by %globaltimer); if it runs
-// out the CTA records a fault in a device word (read by osr_device_fault),
-// waits once more for its own copies, skips its stores and still takes part
-// in the cluster barriers, so no peer is left waiting.
+// The exchange needs no cluster barrier after the start: a CTA leaves once
+// it has received all cs states, and every peer has then already written
+// into it; each CTA writes to a peer only before that peer can leave.  Both
+// waits are bounded (%globaltimer: 1 s for the copies, 2 s for the states);
+// if one runs out the CTA records a fault in a device word (read by
+// osr_device_fault), waits once more for its own copies and skips its
+// stores.  Measured against exchanging through the cluster barrier (arrive
+// release, wait acquire, read peers, arrive again, wait before exit):
+// 6-14 % faster on every staged shape, e.g. 441 x 152064 fp32 87.3 ->
+// 81.6 us, 441 x 152064 bf16 -> fp32 77.5 -> 67.4 us.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -71,11 +77,21 @@ __global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(cons
     const int ns = n - nr;                        // and staged in shared memory
     const char *src = reinterpret_cast<const char *>(a.x) + (row * nunits + u0) * 16;
 
+    // exchange of the CTAs' (m, d): each CTA stores its state into slot
+    // [its rank] of every CTA of the cluster (st.async, counted on the
+    // receiver's xbar), so no CTA waits on a cluster barrier and none has to
+    // outlive its peers' reads
+    __shared__ __align__(8) uint64_t xbar_word;
+    __shared__ float2 xslot[kStagedMaxCluster];
+    const uint32_t xbar = smem_u32(&xbar_word);
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
+        mbar_init(xbar, 1);
+        mbar_arrive_expect_tx(xbar, (uint32_t)a.cs * 8u);
         fence_mbar_init();
     }
     __syncthreads();
+    cluster_arrive_relaxed();  // this CTA's barriers are initialised
     pdl_wait();
     const bool arrive = (a.flags & kFlagNoArrive) == 0;
     if (threadIdx.x == 0 && arrive) {
@@ -136,9 +152,29 @@ __global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(cons
         dt = 0.f;
     }
     __shared__ float red_m[32], red_d[32];
-    __shared__ float2 slot;
     RowNorm rn = block_norm<T / 32>(mt, dt, red_m, red_d);
-    rn = cluster_norm(mt, rn, a.cs, &slot);
+    cluster_wait_acquire();  // every peer's xbar is initialised
+    if (threadIdx.x < a.cs) {
+        const uint32_t me = cluster_ctarank();
+        st_async_f2(mapa_shared(smem_u32(&xslot[me]), threadIdx.x), mapa_shared(xbar, threadIdx.x), rn.m, rn.d);
+    }
+    if (!mbar_wait_bounded(xbar, 0, 2 * kWaitLimitNs)) {
+        atomicOr(&g_staged_fault, 2u);
+        ok = false;
+    }
+    {
+        // lane r (and r + 16) takes CTA r's state: the same fixed order in
+        // every CTA, so all pieces of a row scale by the same (m, d)
+        const int from = threadIdx.x & 15;
+        float pm = -FLT_MAX, pd = 0.f;
+        if (from < a.cs) {
+            const float2 q = xslot[from];
+            pm = q.x;
+            pd = q.y;
+        }
+        rn.m = group_max<16>(pm);
+        rn.d = group_sum<16>(pd * expf(pm - rn.m));
+    }
 
     if (ok) {
         if (a.row_max != nullptr && threadIdx.x == 0 && u0 == 0) {
@@ -168,7 +204,6 @@ __global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(cons
         }
     }
     pdl_trigger();
-    cluster_wait_acquire();
 }
 
 namespace {

@@ -20,6 +20,7 @@ constexpr int kStagedRegUnits = 8;             // ... this many units a thread (
 constexpr int kStagedPreferBytes = 96 << 10;   // piece size that leaves room for 2 CTAs/SM
 constexpr int kStagedMaxSmem = 200 << 10;      // largest staged piece + header
 constexpr int kStagedRegPieceBytes = 76 << 10; // largest piece when part of it is in registers
+constexpr int kStagedMaxCluster = 16;          // CTAs per row at most
 
 // Whether (threads, ru) is one of the compiled kernel shapes.
 constexpr bool staged_shape_ok(int threads, int ru) {
