@@ -111,26 +111,33 @@ int64_t pow2_at_least(int64_t v) {
     return c;
 }
 
-// Whether the staged tier holds part of each piece in registers by default.
-bool staged_regs(osr_dtype in_dt, osr_dtype out_dt) { return !(in_dt == OSR_BF16 && out_dt == OSR_F32); }
+// Whether the staged tier holds part of each piece in registers by default:
+// fp32 input.  Measured over 16 shapes (fp32 rows of 24 Ki to 148 Ki
+// elements, bfloat16 rows of 20 Ki to 148 Ki, 1 to 8192 rows): with
+// registers fp32 rows ran up to 9 % faster (64 x 152064: 17.7 -> 16.2 us),
+// bfloat16 rows 1-20 % slower.
+bool staged_regs(osr_dtype in_dt, osr_dtype out_dt) {
+    (void)out_dt;
+    return in_dt == OSR_F32;
+}
 
 // Staged tier shape.
 //
-// regs (the default except for bfloat16 in, fp32 out): each thread holds
-// kStagedRegUnits units in registers and the rest of its piece is staged.
-// The fewest pieces of at most 76 KiB (about half in registers, so four CTAs
-// fit an SM); with fewer CTAs than SMs, 12 pieces (16 for one or two rows).
-// Measured against the shared-memory-only shapes below on fp32 rows of
-// 24 Ki to 256 Ki elements and bfloat16 rows of 20 Ki to 148 Ki: 0-26 %
-// faster (441 x 152064 fp32: 96.2 -> 87.6 us; 2048 x 32768 bf16: 52.6 ->
-// 48.9 us); bfloat16 -> fp32 rows ran 2-15 % slower with registers.
+// regs: each thread holds kStagedRegUnits units in registers and the rest of
+// its piece is staged.  The fewest pieces of at most 76 KiB (about half in
+// registers, so four CTAs fit an SM); with fewer CTAs than SMs, 12 pieces
+// (16 for one or two rows).
 //
 // Without registers: few rows (three CTAs per SM would need 8 or more per
 // row): 12 CTAs per row, 16 for one or two rows.  Otherwise the fewest CTAs
-// whose pieces fit 96 KiB (or, failing that, 200 KiB), raised toward three
-// CTAs per SM, at least 8 for rows of 192 KiB or more, and rounded up to a
-// power of two, which packs the GPCs better (measured: 152064-element rows
-// ran 13 % faster as 8 pieces than as 7).
+// whose pieces fit 48 KiB (four CTAs an SM; or, failing that, 200 KiB),
+// raised toward three CTAs per SM, at least 8 for rows of 192 KiB or more,
+// and rounded up to a power of two, which packs the GPCs better (measured:
+// 152064-element rows ran 13 % faster as 8 pieces than as 7).  With the
+// barrier-free exchange 48 KiB pieces beat 96 KiB ones by up to 16 %
+// (1024 x 49152 bf16: 40.8 -> 34.3 us).
+//
+// The best shape is within 5 % of these on every measured case.
 //
 // force_cs: 0 decide; force_ru: -1 decide.  Returns false if no piece within
 // the limits holds the row.
