@@ -279,6 +279,20 @@ __device__ __forceinline__ void st_async_f2(uint32_t addr, uint32_t remote_bar, 
                  : "memory");
 }
 
+// The same for four 32-bit words (16 bytes, 16-byte aligned addresses).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t remote_bar, uint4 v) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// The same for one 64-bit word (8-byte aligned address).
+__device__ __forceinline__ void st_async_u64(uint32_t addr, uint32_t remote_bar, uint64_t v) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(addr), "l"(v),
+                 "r"(remote_bar)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copies
 // 1-D bulk asynchronous copies (the TMA engine, no tensor map) from global
 // into this CTA's shared memory, completed through an mbarrier's

@@ -56,6 +56,21 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
     const int64_t nunits = a.N / U;
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+    // cluster: each CTA stores its (m, d, index) into slot [its rank] of
+    // every CTA (st.async, counted on the receiver's xbar); no cluster
+    // barrier after this start-up one
+    __shared__ __align__(8) uint64_t xbar_word;
+    __shared__ uint4 xslot[16];
+    const uint32_t xbar = smem_u32(&xbar_word);
+    if constexpr (CLUSTER) {
+        if (threadIdx.x == 0) {
+            mbar_init(xbar, 1);
+            mbar_arrive_expect_tx(xbar, (uint32_t)a.cs * 16u);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        cluster_arrive_relaxed();  // this CTA's xbar is initialised
+    }
     pdl_wait();
 
     MaxArgSum t{-FLT_MAX, 0.f, kNoIndex};
@@ -122,36 +137,34 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
         r.i = group_min_i64<NW>(s_i[lane & (NW - 1)]);
     }
     if constexpr (CLUSTER) {
-        // CTA results through distributed shared memory; every warp reduces
-        // the cs of them (lanes r and r + 16 read CTA r)
-        __shared__ float2 slot_md;
-        __shared__ long long slot_i;
-        if (threadIdx.x == 0) {
-            slot_md = make_float2(r.m, r.d);
-            slot_i = r.i;
+        cluster_wait_acquire();  // every peer's xbar is initialised
+        if (threadIdx.x < a.cs) {
+            const uint4 v = make_uint4(__float_as_uint(r.m), __float_as_uint(r.d), (uint32_t)r.i,
+                                       (uint32_t)((uint64_t)r.i >> 32));
+            st_async_v4(mapa_shared(smem_u32(&xslot[cluster_ctarank()]), threadIdx.x),
+                        mapa_shared(xbar, threadIdx.x), v);
         }
-        cluster_arrive_release();
-        cluster_wait_acquire();
+        // bounded (2 s): a state that never arrives gives NaN and -1
+        const bool got = mbar_wait_bounded(xbar, 0, 2000000000ull);
+        // lanes q and q + 16 take CTA q's state, the same order in every CTA
         const int q = threadIdx.x & 15;
         MaxArgSum p{-FLT_MAX, 0.f, kNoIndex};
         if (q < a.cs) {
-            const float2 md = ld_dsmem_f2(mapa_shared(smem_u32(&slot_md), q));
-            long long pi;
-            asm volatile("ld.shared::cluster.s64 %0, [%1];"
-                         : "=l"(pi)
-                         : "r"(mapa_shared(smem_u32(&slot_i), q))
-                         : "memory");
-            p = MaxArgSum{md.x, md.y, pi};
+            const uint4 v = xslot[q];
+            p = MaxArgSum{__uint_as_float(v.x), __uint_as_float(v.y),
+                          (int64_t)(((uint64_t)v.w << 32) | v.z)};
         }
         r = group_mas<16>(p);
-        cluster_arrive_relaxed();
+        if (!got) {
+            r.m = __int_as_float(0x7fffffff);
+            r.i = kNoIndex;
+        }
     }
     if (s.ok && s.t == 0 && s.u0 == 0) {
         if (a.row_sum != nullptr) a.row_sum[s.row] = r.m + logf(r.d);
         if (a.row_arg != nullptr) a.row_arg[s.row] = r.i == kNoIndex ? -1 : r.i;
     }
     pdl_trigger();
-    if constexpr (CLUSTER) cluster_wait_acquire();
 }
 
 namespace {

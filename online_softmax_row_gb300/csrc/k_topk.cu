@@ -23,19 +23,23 @@
 //              short list as a (key, column) word (keys: an order-preserving
 //              integer map, -0 as +0, NaN above every number; words order by
 //              key, then by smaller column, and all differ);
-//   merge   -- one cluster exchange: the row's (m, d) by the (m, d) merge of
-//              the CTAs' (lse = m + log d), and the lists' lengths;
-//   select  -- CTA 0 gathers the union of the lists (it holds every element
-//              at or above the k-th largest), finds the k-th largest key T by
+//   merge   -- one exchange: each CTA stores its (m, d) and list length
+//              into every CTA (st.async, counted on the receiver's
+//              mbarrier); the row's (m, d) by the (m, d) merge of the CTAs'
+//              (lse = m + log d);
+//   select  -- every CTA stores its list into CTA 0 the same way, and CTA 0,
+//              with the union of the lists (it holds every element at or
+//              above the k-th largest), finds the k-th largest key T by
 //              8-bit radix passes over it, takes the words above T and the
 //              largest of those equal to T, and writes them in order (values
 //              re-read from the row, columns, the softmax of the k values).
 // When a list overflows (k > 256 gives no bound; heavy ties at the bound) or
 // the union does not fit, the cluster selects together instead: radix passes
 // over the lists or the whole pieces with the histograms summed through
-// distributed shared memory each pass, and the equal keys shared out by a
-// prefix over the CTAs.  The result is unique (a total order), so it is
-// deterministic.
+// distributed shared memory each pass (behind cluster barriers), and the
+// equal keys shared out by a prefix over the CTAs.  The result is unique (a
+// total order), so it is deterministic.  The exchanges' waits are bounded
+// (2 s); one that runs out writes NaN / -1 for the row.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -222,11 +226,15 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
     __shared__ float s_red[kWarps], s_gw[kWarps];
     __shared__ uint32_t s_scan[kWarps];
     __shared__ float s_ez[kTopkRankMaxK];
-    __shared__ float pub_m, pub_d;
-    __shared__ uint32_t pub_n, pub_cand, list_n, s_bin, s_krem;
-    __shared__ float s_rm[kTopkMaxCluster], s_rd[kTopkMaxCluster];
-    __shared__ uint32_t s_rn[kTopkMaxCluster], s_off[kTopkMaxCluster + 1];
+    __shared__ uint32_t pub_cand, list_n, s_bin, s_krem;
+    __shared__ uint32_t s_off[kTopkMaxCluster + 1];
     __shared__ uint64_t s_top;
+    // exchanges without a cluster barrier: st.async into the receiver's
+    // shared memory, counted on its mbarrier.  xbar[0]: every CTA's
+    // (m, d, list length) into xstate[its rank] of every CTA; xbar[1]: on
+    // the short path, every CTA's list into CTA 0's union
+    __shared__ __align__(8) uint64_t xbar_words[2];
+    __shared__ uint4 xstate[kTopkMaxCluster];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cs = a.cs;
@@ -263,10 +271,17 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         }
     };
 
+    const uint32_t xbar0 = smem_u32(&xbar_words[0]), xbar1 = smem_u32(&xbar_words[1]);
     if (tid == 0) {
         pub_cand = 0;
         list_n = 0;
+        mbar_init(xbar0, 1);
+        mbar_init(xbar1, 1);
+        mbar_arrive_expect_tx(xbar0, (uint32_t)cs * 16u);
+        fence_mbar_init();
     }
+    __syncthreads();
+    cluster_arrive_relaxed();  // this CTA's barriers are initialised
     pdl_wait();
 
     // ---- load the piece (the row is read from HBM once, every copy in
@@ -330,29 +345,36 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
     });
     dt = block_sum_f(dt, s_red);  // also orders the list appends
     const uint32_t nl = list_n;
-    if (tid == 0) {
-        pub_m = mc;
-        pub_d = dt;
-        pub_n = nl;
-    }
 
     // ---- exchange: the row's (m, d) by the merge of the CTAs' (m, d), and
-    //      the lists' lengths (thread r reads CTA r's, all at once)
-    cluster_sync_all();
-    if (tid < cs) {
-        s_rm[tid] = ld_dsmem_f32(mapa_shared(smem_u32(&pub_m), tid));
-        s_rd[tid] = ld_dsmem_f32(mapa_shared(smem_u32(&pub_d), tid));
-        s_rn[tid] = ld_dsmem_u32(mapa_shared(smem_u32(&pub_n), tid));
+    //      the lists' lengths
+    cluster_wait_acquire();  // every peer's barriers are initialised
+    if (tid < cs)
+        st_async_v4(mapa_shared(smem_u32(&xstate[rank]), tid), mapa_shared(xbar0, tid),
+                    make_uint4(__float_as_uint(mc), __float_as_uint(dt), nl, 0u));
+    auto fail = [&]() {  // a state or list that never arrived (bounded waits: 2 s)
+        for (int64_t t = tid; rank == 0 && t < k; t += kTopkThreads) {
+            a.values[row * k + t] = __uint_as_float(0x7fc00000u);
+            a.indices[row * k + t] = -1;
+            if (a.probs != nullptr) a.probs[row * k + t] = __uint_as_float(0x7fc00000u);
+        }
+        if (rank == 0 && tid == 0 && a.lse != nullptr) a.lse[row] = __uint_as_float(0x7fc00000u);
+        pdl_trigger();
+    };
+    if (!__syncthreads_and(mbar_wait_bounded(xbar0, 0, 2000000000ull))) {
+        fail();
+        return;
     }
-    __syncthreads();
     float m = -FLT_MAX, d = 0.f;
     uint32_t over = 0, total = 0;
     for (int r = 0; r < cs; ++r) {
-        m = fmaxf(m, s_rm[r]);
-        over |= s_rn[r] > (uint32_t)kTopkListCap;
-        total += s_rn[r] < (uint32_t)kTopkListCap ? s_rn[r] : (uint32_t)kTopkListCap;
+        const uint32_t rn = xstate[r].z;
+        m = fmaxf(m, __uint_as_float(xstate[r].x));
+        over |= rn > (uint32_t)kTopkListCap;
+        total += rn < (uint32_t)kTopkListCap ? rn : (uint32_t)kTopkListCap;
     }
-    for (int r = 0; r < cs; ++r) d += s_rd[r] * expf(s_rm[r] - m);
+    for (int r = 0; r < cs; ++r)
+        d += __uint_as_float(xstate[r].y) * expf(__uint_as_float(xstate[r].x) - m);
     if (rank == 0 && a.lse != nullptr && tid == 0) a.lse[row] = m + logf(d);
 
     auto value_at = [&](uint32_t j) {  // the row's own value (an index outside
@@ -407,36 +429,20 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
     if (!over && total <= a.region0 / 8) {
         // ---- the short path: the union of the lists holds every element at
         //      or above the k-th largest (each CTA's bound lies below it).
-        //      CTA 0 gathers the union and selects from it alone.
-        if (rank == 0) {
-            // word i of the union: list of CTA r, entry i - s_off[r]
-            if (tid == 0) {
-                s_off[0] = 0;
-                for (int r = 0; r < cs; ++r) s_off[r + 1] = s_off[r] + s_rn[r];
-            }
-            __syncthreads();
-            for (uint32_t i0 = tid; i0 < total; i0 += 4 * kTopkThreads) {
-                uint64_t v[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t i = i0 + j * kTopkThreads;
-                    v[j] = 0ull;
-                    if (i < total) {
-                        int r = 0;
-                        while (i >= s_off[r + 1]) ++r;
-                        v[j] = ld_dsmem_u64(mapa_shared(smem_u32(list + (i - s_off[r])), r));
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t i = i0 + j * kTopkThreads;
-                    if (i < total) words[i] = v[j];
-                }
-            }
-        }
-        cluster_sync_all();  // no CTA leaves while CTA 0 reads its list
+        //      Every CTA stores its list into CTA 0's union (which reuses the
+        //      piece region, no longer read once the states went out); CTA 0
+        //      selects from it alone.
+        uint32_t off = 0;
+        for (int r = 0; r < (int)rank; ++r) off += xstate[r].z;
+        if (rank == 0 && tid == 0) mbar_arrive_expect_tx(xbar1, total * 8u);
+        const uint32_t to_words = mapa_shared(smem_u32(words + off), 0), to_bar = mapa_shared(xbar1, 0);
+        for (uint32_t i = tid; i < nl; i += kTopkThreads) st_async_u64(to_words + i * 8u, to_bar, list[i]);
         if (rank != 0) {
             pdl_trigger();
+            return;
+        }
+        if (!__syncthreads_and(mbar_wait_bounded(xbar1, 0, 2000000000ull))) {
+            fail();
             return;
         }
         __syncthreads();
