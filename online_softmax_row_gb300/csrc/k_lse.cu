@@ -24,6 +24,7 @@ constexpr int64_t kNoIndex = 0x7fffffffffffffffLL;
 // elements per thread per tile: twice the row kernels' 16, so each thread
 // keeps 64 (bf16) to 128 (fp32) bytes of loads in flight in a streaming loop
 constexpr int kLseEpt = 32;
+constexpr int kLseStagedHeader = 128;  // the copies' mbarrier, padded
 
 template <int W>
 __device__ __forceinline__ int64_t group_min_i64(int64_t v) {
@@ -167,6 +168,116 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
     pdl_trigger();
 }
 
+// Staged variant for rows spread over a cluster (16-byte rows): each CTA
+// bulk-copies its whole piece into shared memory at once (every byte in
+// flight together, where the streaming kernel above waits for one tile of
+// loads after another), then takes its maximum with the first index holding
+// it, and its sum of exp(x - max), from shared memory.  The CTAs' (m, d,
+// index) go to every CTA of the cluster by st.async, as above.
+template <Dt DI>
+__global__ void __launch_bounds__(256) lse_staged_kernel(const RowArgs a) {
+    constexpr int U = Elem<DI>::kVec;
+    constexpr int T = 256;
+    constexpr int NW = T / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t bar = smem_u32(smem);
+    const unsigned char *stage = smem + kLseStagedHeader;
+    __shared__ __align__(8) uint64_t xbar_word;
+    __shared__ uint4 xslot[16];
+    __shared__ float s_m[NW], s_d[NW];
+    __shared__ long long s_i[NW];
+    const uint32_t xbar = smem_u32(&xbar_word);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    const int64_t nunits = a.N / U;
+    const int64_t row = blockIdx.x / a.cs;
+    const uint32_t rank = cluster_ctarank();
+    const int64_t u0 = (int64_t)rank * a.chunk;
+    const int64_t u1 = u0 + a.chunk < nunits ? u0 + a.chunk : nunits;
+    const int n = u1 > u0 ? (int)(u1 - u0) : 0;
+    const char *src = reinterpret_cast<const char *>(a.x) + (row * nunits + u0) * 16;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        mbar_init(xbar, 1);
+        mbar_arrive_expect_tx(xbar, (uint32_t)a.cs * 16u);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();  // this CTA's barriers are initialised
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        const uint64_t policy = l2_evict_first_policy();  // read once
+        const uint32_t bytes = (uint32_t)n * 16u;
+        mbar_arrive_expect_tx(bar, bytes);
+        for (uint32_t off = 0; off < bytes; off += 32768u) {
+            const uint32_t len = bytes - off < 32768u ? bytes - off : 32768u;
+            bulk_load_g2s_hint(smem_u32(stage) + off, src + off, len, bar, policy);
+        }
+    }
+    bool ok = __syncthreads_and(mbar_wait_bounded(bar, 0, 1000000000ull));
+    if (!ok) mbar_wait_bounded(bar, 0, 1000000000ull);  // own copies still landing
+
+    // the CTA's maximum and the first index holding it (each thread visits
+    // its elements in increasing index order; NaN never wins), then its sum
+    float tm = -FLT_MAX;
+    int64_t ti = kNoIndex;
+    if (ok) {
+        for (int u = threadIdx.x; u < n; u += T) {
+            float v[U];
+            load_unit<DI, U, Hint::Keep>(stage, (int64_t)u * U, v);
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+                if (v[k] > tm) {
+                    tm = v[k];
+                    ti = (u0 + u) * U + k;
+                }
+        }
+    }
+    float m = group_max<32>(tm);
+    if (lane == 0) s_m[warp] = m;
+    __syncthreads();
+    m = group_max<NW>(s_m[lane & (NW - 1)]);
+    const int64_t wi = group_min_i64<32>(tm == m ? ti : kNoIndex);
+    float td = 0.f;
+    if (ok) {
+        for (int u = threadIdx.x; u < n; u += T) {
+            float v[U];
+            load_unit<DI, U, Hint::Keep>(stage, (int64_t)u * U, v);
+#pragma unroll
+            for (int k = 0; k < U; ++k) td += exp_shifted(v[k], m);
+        }
+    }
+    const float wd = group_sum<32>(td);
+    if (lane == 0) {
+        s_d[warp] = wd;
+        s_i[warp] = wi;
+    }
+    __syncthreads();
+    MaxArgSum r{m, group_sum<NW>(s_d[lane & (NW - 1)]), group_min_i64<NW>(s_i[lane & (NW - 1)])};
+
+    cluster_wait_acquire();  // every peer's xbar is initialised
+    if (threadIdx.x < a.cs) {
+        const uint4 v = make_uint4(__float_as_uint(r.m), __float_as_uint(r.d), (uint32_t)r.i,
+                                   (uint32_t)((uint64_t)r.i >> 32));
+        st_async_v4(mapa_shared(smem_u32(&xslot[rank]), threadIdx.x), mapa_shared(xbar, threadIdx.x), v);
+    }
+    ok = mbar_wait_bounded(xbar, 0, 2000000000ull) && ok;
+    const int q = threadIdx.x & 15;
+    MaxArgSum p{-FLT_MAX, 0.f, kNoIndex};
+    if (q < a.cs) {
+        const uint4 v = xslot[q];
+        p = MaxArgSum{__uint_as_float(v.x), __uint_as_float(v.y), (int64_t)(((uint64_t)v.w << 32) | v.z)};
+    }
+    r = group_mas<16>(p);
+    if (threadIdx.x == 0 && u0 == 0) {
+        // a copy or state that never arrived (bounded waits) gives NaN and -1
+        if (a.row_sum != nullptr) a.row_sum[row] = ok ? r.m + logf(r.d) : __int_as_float(0x7fffffff);
+        if (a.row_arg != nullptr) a.row_arg[row] = ok && r.i != kNoIndex ? r.i : -1;
+    }
+    pdl_trigger();
+}
+
 namespace {
 
 using KernelFn = void (*)(RowArgs);
@@ -216,6 +327,29 @@ cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cu
 }  // namespace
 
 template <Dt DI>
+cudaError_t launch_lse_staged(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st) {
+    const KernelFn fn = lse_staged_kernel<DI>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && a.cs > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)a.cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+template <Dt DI>
 cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t grid,
                        cudaStream_t st) {
     if (vec) return launch_lse_u<DI, Elem<DI>::kVec>(a, g, cluster, grid, st);
@@ -224,5 +358,7 @@ cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t 
 
 template cudaError_t launch_lse<Dt::F32>(const RowArgs &, int, bool, bool, int64_t, cudaStream_t);
 template cudaError_t launch_lse<Dt::BF16>(const RowArgs &, int, bool, bool, int64_t, cudaStream_t);
+template cudaError_t launch_lse_staged<Dt::F32>(const RowArgs &, int64_t, size_t, cudaStream_t);
+template cudaError_t launch_lse_staged<Dt::BF16>(const RowArgs &, int64_t, size_t, cudaStream_t);
 
 }  // namespace osr

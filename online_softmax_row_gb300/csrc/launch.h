@@ -94,5 +94,9 @@ cudaError_t rmsnorm_cluster_occupancy(int g, bool vec, int cs, int *n);
 template <Dt DI>
 cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t grid,
                        cudaStream_t st);
+// Staged variant (16-byte rows): a.cs CTAs per row, each bulk-copying its
+// piece of a.chunk units into `smem` bytes of shared memory (128 + piece).
+template <Dt DI>
+cudaError_t launch_lse_staged(const RowArgs &a, int64_t grid, size_t smem, cudaStream_t st);
 
 }  // namespace osr

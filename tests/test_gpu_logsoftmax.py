@@ -157,10 +157,32 @@ def test_log_softmax_vocab_workload_full_size():
     check_log(x, y)
 
 
-@pytest.mark.parametrize("cs", [2, 3, 10, 12, 16])
-def test_logsumexp_forced_cluster_sizes(cs):
-    x = case(6, 152064, "bf16", seed_of("lse-cs", cs))
-    os.environ["OSR_FORCE_KERNEL"] = f"lse:cs={cs}"
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_row_logsumexp_staged_edges(dt):
+    # few rows: pieces staged in shared memory; a -inf row, a NaN, ties split
+    # over CTAs, and a row whose maximum sits in the last piece
+    N = 65536
+    x = torch.randn(4, N, generator=torch.Generator().manual_seed(17)) * 3
+    x[0] = -float("inf")
+    x[1, 40000] = float("nan")
+    x[2, 9] = 50.0
+    x[2, N - 3] = 50.0
+    x[3, N - 1] = 60.0
+    x = x.to(DT[dt])
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 4, N, dt).startswith("lse-staged")
+    lse, am = osr.row_logsumexp(x.cuda())
+    lse, am = lse.cpu(), am.cpu()
+    assert am.tolist()[0] == -1 and lse[0] == -float("inf")
+    assert torch.isnan(lse[1]) and am[1] == int(torch.argmax(torch.nan_to_num(x[1].float(), nan=-1e30)))
+    assert am.tolist()[2:] == [9, N - 1]
+    check_lse(x[2:], lse[2:], am[2:])
+
+
+@pytest.mark.parametrize("spec", ["lse:cs=2", "lse:cs=3", "lse:cs=10", "lse:cs=12", "lse:cs=16",
+                                  "lse:cs=4,st=0", "lse:cs=10,st=0"])
+def test_logsumexp_forced_cluster_sizes(spec):
+    x = case(6, 152064, "bf16", seed_of("lse-cs", spec))
+    os.environ["OSR_FORCE_KERNEL"] = spec
     try:
         lse, am = osr.row_logsumexp(x.cuda())
         torch.cuda.synchronize()
