@@ -18,27 +18,11 @@ namespace osr {
 //   y = ((x - p) - mu_s) * rsqrt(var + eps) * gamma + beta.
 // On 16-byte rows the arithmetic runs on binary32 pairs (f32x2), a quarter
 // fewer instructions: the kernel is issue-bound, not memory-bound, with the
-// scalar form.  Cluster tier: both sums are taken across the cluster's CTAs through
-// distributed shared memory, two exchanges with one barrier each.  (Merging
-// per-thread (n, mean, M2) states with Chan's formula in a single reduction
-// measured 28 % slower: its divisions cost more than the second barrier.)
-__device__ __forceinline__ float cluster_gather_sum(float v, int cs, float *slot) {
-    if (threadIdx.x == 0) *slot = v;
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    const int q = threadIdx.x & 15;
-    float t = 0.f;
-    if (q < cs) {
-        float r;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                     : "=f"(r)
-                     : "r"(mapa_shared(smem_u32(slot), q))
-                     : "memory");
-        t = r;
-    }
-    return group_sum<16>(t);
-}
-
+// scalar form.  Cluster tier: both sums are taken across the cluster's CTAs,
+// each by one barrier-free exchange (cluster_sum).  (Merging per-thread (n,
+// mean, M2) states with Chan's formula in a single reduction measured 28 %
+// slower, with the exchanges behind cluster barriers: its divisions cost
+// more than the second exchange.)
 template <Dt D, int G, int EPT, int U, bool CLUSTER>
 __global__ void __launch_bounds__(RowsGeom<G>::kThreads)
 layernorm_rows_kernel(const RowArgs a) {
@@ -55,6 +39,7 @@ layernorm_rows_kernel(const RowArgs a) {
     const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
     const char *gam = reinterpret_cast<const char *>(a.gamma);
     const char *bet = reinterpret_cast<const char *>(a.beta);
+    if constexpr (CLUSTER) cluster_push_init(cluster_push_area<0>(), cluster_push_area<1>(), a.cs);
     pdl_wait();
 
     float p = 0.f;  // pivot: x[row][0]
@@ -114,13 +99,12 @@ layernorm_rows_kernel(const RowArgs a) {
             if (valid >> j & 1u) s1 += v[j] - p;
     }
     __shared__ float red1[32], red2[32];
-    __shared__ float slot1, slot2;
     if constexpr (G <= 32) {
         s1 = group_sum<G>(s1);
     } else {
         s1 = block_sum<RowsGeom<G>::kWarps>(s1, red1);
     }
-    if constexpr (CLUSTER) s1 = cluster_gather_sum(s1, a.cs, &slot1);
+    if constexpr (CLUSTER) s1 = cluster_sum(s1, a.cs, cluster_push_area<0>(), true);
     const float mu = s1 / (float)a.N;  // mean of the shifted values
     const uint64_t mu2 = f2_make(mu, mu);
 
@@ -151,10 +135,7 @@ layernorm_rows_kernel(const RowArgs a) {
     } else {
         s2 = block_sum<RowsGeom<G>::kWarps>(s2, red2);
     }
-    if constexpr (CLUSTER) {
-        s2 = cluster_gather_sum(s2, a.cs, &slot2);
-        cluster_arrive_relaxed();
-    }
+    if constexpr (CLUSTER) s2 = cluster_sum(s2, a.cs, cluster_push_area<1>(), false);
     const float r = rsqrtf(s2 / (float)a.N + a.eps);
     const uint64_t r2 = f2_make(r, r);
 
@@ -193,7 +174,6 @@ layernorm_rows_kernel(const RowArgs a) {
         }
     }
     pdl_trigger();
-    if constexpr (CLUSTER) cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------ LayerNorm, split

@@ -26,6 +26,7 @@ rmsnorm_rows_kernel(const RowArgs a) {
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const int64_t row_off = s.row * a.N * Elem<D>::kBytes;
     const char *xrow = reinterpret_cast<const char *>(a.x) + row_off;
+    if constexpr (CLUSTER) cluster_push_init(cluster_push_area<0>(), nullptr, a.cs);
     pdl_wait();
 
     uint4 pk[NP], gp[NP];
@@ -107,10 +108,7 @@ rmsnorm_rows_kernel(const RowArgs a) {
         __shared__ float red[32];
         ss = block_sum<RowsGeom<G>::kWarps>(ss, red);
     }
-    if constexpr (CLUSTER) {
-        __shared__ float2 slot;
-        ss = cluster_sum(ss, a.cs, &slot);
-    }
+    if constexpr (CLUSTER) ss = cluster_sum(ss, a.cs, cluster_push_area<0>(), true);
     const float r = rsqrtf(ss / (float)a.N + a.eps);
 
     char *yrow = reinterpret_cast<char *>(a.y) + row_off;
@@ -134,7 +132,6 @@ rmsnorm_rows_kernel(const RowArgs a) {
         }
     }
     pdl_trigger();
-    if constexpr (CLUSTER) cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------ RMSNorm pass 1

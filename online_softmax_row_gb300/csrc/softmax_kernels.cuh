@@ -20,6 +20,7 @@ softmax_rows_kernel(const RowArgs a) {
     const int64_t nunits = a.N / U;
     const Slice s = make_slice<G, CLUSTER>(a, nunits);
     const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+    if constexpr (CLUSTER) cluster_push_init(cluster_push_area<0>(), nullptr, a.cs);
     pdl_wait();
 
     float v[NU][U];
@@ -58,10 +59,7 @@ softmax_rows_kernel(const RowArgs a) {
         __shared__ float red_m[32], red_d[32];
         rn = block_norm<RowsGeom<G>::kWarps>(mt, dt, red_m, red_d);
     }
-    if constexpr (CLUSTER) {
-        __shared__ float2 slot;
-        rn = cluster_norm(mt, rn, a.cs, &slot);
-    }
+    if constexpr (CLUSTER) rn = cluster_norm(mt, rn, a.cs, cluster_push_area<0>(), true);
 
     const float scale = rn.f / rn.d;
     const float logd = logf(rn.d);
@@ -82,7 +80,6 @@ softmax_rows_kernel(const RowArgs a) {
         }
     }
     pdl_trigger();
-    if constexpr (CLUSTER) cluster_wait_acquire();
 }
 
 // ------------------------------------------------------------ softmax pass 1
