@@ -130,18 +130,17 @@ bool staged_regs(osr_dtype in_dt, osr_dtype out_dt) {
 //
 // Without registers: few rows (three CTAs per SM would need 8 or more per
 // row): 12 CTAs per row, 16 for one or two rows.  Otherwise the fewest CTAs
-// whose pieces fit 48 KiB (four CTAs an SM; or, failing that, 200 KiB),
-// raised toward three CTAs per SM, at least 8 for rows of 192 KiB or more,
-// and rounded up to a power of two, which packs the GPCs better (measured:
-// 152064-element rows ran 13 % faster as 8 pieces than as 7).  With the
-// barrier-free exchange 48 KiB pieces beat 96 KiB ones by up to 16 %
-// (1024 x 49152 bf16: 40.8 -> 34.3 us).
+// that each read and write at most 80 KiB (at most 16 CTAs), raised toward
+// three CTAs per SM; above 8, rounded to a multiple of 4.  Measured on bf16 rows of
+// 20 Ki to 256 Ki elements, to bf16 and to fp32: within 5 % of the best
+// cluster size, where 48 KiB pieces rounded to a power of two (the rule
+// before the barrier-free exchange) were up to 16 % off.
 //
 // The best shape is within 5 % of these on every measured case.
 //
 // force_cs: 0 decide; force_ru: -1 decide.  Returns false if no piece within
 // the limits holds the row.
-bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, bool regs,
+bool staged_shape(int64_t M, int64_t nunits, int64_t io_row_bytes, int sms, int max_cluster, bool regs,
                   int64_t force_cs, int64_t force_ru, int64_t force_g, Plan *p) {
     const int64_t row_bytes = nunits * 16;
     const int64_t ru = force_ru >= 0 ? force_ru : regs ? kStagedRegUnits : 0;
@@ -156,8 +155,8 @@ bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, bool regs
         if (cs > max_cluster) cs = max_cluster;
         if (cs > most) cs = most;
     } else if (cs <= 0) {
-        int64_t need = cdiv(row_bytes, kStagedPreferBytes);
-        if (need > max_cluster) need = cdiv(row_bytes, kStagedMaxSmem - 128);
+        int64_t need = cdiv(io_row_bytes, kStagedPieceIoBytes);
+        if (need > max_cluster) need = max_cluster;  // the smallest pieces there are
         int64_t fill = cdiv(3 * (int64_t)sms, M);
         if (fill >= 8 && need <= 12) {
             // few rows: spread each row wide.  Measured on 1..64 rows of 64 Ki
@@ -165,18 +164,21 @@ bool staged_shape(int64_t M, int64_t nunits, int sms, int max_cluster, bool regs
             // (5-18 % faster than 8 or 16, e.g. 64 vocabulary rows 16.7 ->
             // 15.8 us); larger clusters pay more than their extra bandwidth
             cs = M <= 2 ? 16 : 12;
-            if (cs > max_cluster) cs = max_cluster;
-            if (cs > most) cs = most;
         } else {
             if (fill > most) fill = most;
             if (fill > max_cluster) fill = max_cluster;
             cs = need > fill ? need : fill;
-            // rows of 192 KiB and more: at least 8 pieces, so a wave holds
-            // enough CTAs (measured 4-10 % faster than 4 pieces at 128-256 rows)
-            if (row_bytes >= (192 << 10) && cs < 8) cs = 8;
-            const int64_t c2 = pow2_at_least(cs);
-            if (c2 <= max_cluster && cdiv(nunits, c2) >= kStagedThreads / 4) cs = c2;
+            // above 8, the nearest multiple of 4 that still fits: clusters
+            // of 12 packed better than 10, 11 or 13 (128 x 262144 bf16:
+            // 27.0 us at 12, 29.4 at 13)
+            if (cs > 8) {
+                int64_t c4 = (cs + 2) / 4 * 4;
+                while (c4 < max_cluster && 128 + cdiv(nunits, c4) * 16 > kStagedMaxSmem) c4 += 4;
+                cs = c4;
+            }
         }
+        if (cs > max_cluster) cs = max_cluster;
+        if (cs > most) cs = most;
     }
     if (cs < 1 || cs > max_cluster || cs > kStagedMaxCluster) return false;
     const int64_t chunk = cdiv(nunits, cs);
@@ -256,7 +258,8 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
             parse_kv(force, "r", &ru);
             parse_kv(force, "g", &g);
             if (cs <= 0) cs = 0;
-            return staged_shape(M, nunits, sms, max_cluster, staged_regs(in_dt, out_dt), cs, ru, g, p)
+            return staged_shape(M, nunits, N * (in_bytes + elem_bytes(out_dt)), sms, max_cluster,
+                                staged_regs(in_dt, out_dt), cs, ru, g, p)
                        ? OSR_OK
                        : OSR_ERR_UNSUPPORTED;
         }
@@ -284,7 +287,8 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
     // 2. softmax on 16-byte rows: a cluster per row, pieces staged in shared
     //    memory by bulk copies (one read)
     if (op == Op::Softmax && vec &&
-        staged_shape(M, nunits, sms, max_cluster, staged_regs(in_dt, out_dt), 0, -1, 0, p))
+        staged_shape(M, nunits, N * (in_bytes + elem_bytes(out_dt)), sms, max_cluster,
+                     staged_regs(in_dt, out_dt), 0, -1, 0, p))
         return OSR_OK;
     // 3. a cluster of 1024-thread CTAs, still register-cached (one read)
     const int64_t cs = cdiv(nunits, (int64_t)1024 * upt);

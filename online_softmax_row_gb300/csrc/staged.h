@@ -17,7 +17,7 @@ namespace osr {
 constexpr int kStagedThreads = 256;            // shared-memory-only CTAs
 constexpr int kStagedRegThreads = 256;         // CTAs holding part of the piece in registers ...
 constexpr int kStagedRegUnits = 8;             // ... this many units a thread (64 registers)
-constexpr int kStagedPreferBytes = 48 << 10;   // largest piece without registers (4 CTAs/SM)
+constexpr int kStagedPieceIoBytes = 80 << 10;  // bytes a CTA reads and writes, without registers
 constexpr int kStagedMaxSmem = 200 << 10;      // largest staged piece + header
 constexpr int kStagedRegPieceBytes = 76 << 10; // largest piece when part of it is in registers
 constexpr int kStagedMaxCluster = 16;          // CTAs per row at most

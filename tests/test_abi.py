@@ -126,15 +126,17 @@ def test_dispatch_staged_shapes(m, n, want):
 
 
 @pytest.mark.parametrize("m,n,io,want", [
-    # bfloat16 rows stage whole pieces in shared memory: pieces <= 48 KiB,
-    # at least 8 for rows of 192 KiB or more, 2^k
-    (441, 152064, ("bf16", "f32"), "staged cs=8 g=256 piece=38016B vec"),
+    # bfloat16 rows stage whole pieces in shared memory: the fewest CTAs
+    # reading and writing at most 80 KiB each, multiples of 4 above 8
+    (441, 152064, ("bf16", "f32"), "staged cs=12 g=256 piece=25344B vec"),
     (512, 152064, ("bf16", "bf16"), "staged cs=8 g=256 piece=38016B vec"),
+    (128, 262144, ("bf16", "bf16"), "staged cs=12 g=256 piece=43696B vec"),   # 13 -> 12
     (64, 152064, ("bf16", "f32"), "staged cs=12 g=256 piece=25344B vec"),     # few rows: 12 CTAs
-    (2048, 32768, ("bf16", "f32"), "staged cs=2 g=256 piece=32768B vec"),
+    (2048, 32768, ("bf16", "f32"), "staged cs=3 g=256 piece=21856B vec"),
     (2048, 32768, ("bf16", "bf16"), "staged cs=2 g=256 piece=32768B vec"),
-    (1024, 49152, ("bf16", "bf16"), "staged cs=2 g=256 piece=49152B vec"),
+    (1024, 49152, ("bf16", "bf16"), "staged cs=3 g=256 piece=32768B vec"),
     (8192, 20480, ("bf16", "bf16"), "staged cs=1 g=256 piece=40960B vec"),
+    (200, 400000, ("bf16", "f32"), "staged cs=16 g=256 piece=50000B vec"),    # as many as there are
     # fp32 -> bfloat16 holds part in registers like fp32 -> fp32
     (441, 152064, ("f32", "bf16"), "staged cs=8 g=256 piece=76032B r=8 vec"),
 ])
@@ -153,7 +155,7 @@ def test_dispatch_capacity_counts_cached_elements():
     # the norms keep them packed); the split softmax kernels stay at 16
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32") == "rows g=512 ept=32 vec"
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "f32") == "rows g=1024 ept=16 vec"
-    assert osr.plan_describe(osr.OP_SOFTMAX, 2048, 32768, "bf16", "f32") == "staged cs=2 g=256 piece=32768B vec"
+    assert osr.plan_describe(osr.OP_SOFTMAX, 2048, 32768, "bf16", "f32") == "staged cs=3 g=256 piece=21856B vec"
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32").startswith("split")
     assert "ept=16" in osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32")
     assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "rows g=1024 ept=32 vec"
