@@ -100,7 +100,7 @@ def test_bench_copy_validation(lib):
 
 @pytest.mark.parametrize("n,tier", [
     (1, "rows g=1"), (32, "rows g=2"), (128, "rows g=8"), (1024, "rows g=64"),
-    (4096, "rows g=256"), (16384, "rows g=1024"), (32768, "staged cs=12"),
+    (4096, "rows g=256"), (16384, "cluster cs=4 g=256"), (32768, "staged cs=12"),
     (152064, "staged cs=8"), (262144, "staged cs=14"), (1 << 20, "split"),
 ])
 def test_dispatch_tiers_softmax_f32(lib, n, tier):
@@ -145,22 +145,28 @@ def test_dispatch_staged_shapes_by_dtype(m, n, io, want):
 
 
 def test_dispatch_long_rows_without_staging():
-    # norms and misaligned rows keep the register-cached cluster tier
-    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "f32").startswith("cluster cs=2 g=1024")
-    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 32768, "f32", vec_ok=False).startswith("cluster cs=2")
+    # norms and misaligned rows keep the register-cached cluster tier: up to
+    # 16 CTAs of 256 threads, CTAs of 1024 threads beyond that
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "f32") == "cluster cs=8 g=256 ept=16 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 8, 131072, "f32") == "cluster cs=8 g=1024 ept=16 vec"
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 32768, "f32", vec_ok=False) == "cluster cs=8 g=256 ept=16 scalar"
+    # rows that would need a 1024-thread CTA go to four 256-thread CTAs
+    assert osr.plan_describe(osr.OP_RMSNORM, 2048, 16384, "f32") == "cluster cs=4 g=256 ept=16 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 2048, 8192, "f32") == "rows g=512 ept=16 vec"
 
 
 def test_dispatch_capacity_counts_cached_elements():
     # 16-byte bf16 rows: 32 elements a thread (softmax caches them as binary32,
     # the norms keep them packed); the split softmax kernels stay at 16
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "bf16", "f32") == "rows g=512 ept=32 vec"
-    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "f32") == "rows g=1024 ept=16 vec"
+    assert osr.plan_describe(osr.OP_SOFTMAX, 64, 16384, "f32") == "cluster cs=4 g=256 ept=16 vec"
     assert osr.plan_describe(osr.OP_SOFTMAX, 2048, 32768, "bf16", "f32") == "staged cs=3 g=256 piece=21856B vec"
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32").startswith("split")
     assert "ept=16" in osr.plan_describe(osr.OP_SOFTMAX, 64, 1 << 22, "bf16", "f32")
-    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "rows g=1024 ept=32 vec"
-    assert osr.plan_describe(osr.OP_RMSNORM, 64, 65536, "bf16").startswith("cluster cs=2")
-    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32767, "bf16").startswith("cluster cs=2 g=1024 ept=16 scalar")
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 16384, "bf16") == "rows g=512 ept=32 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32768, "bf16") == "cluster cs=4 g=256 ept=32 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 65536, "bf16") == "cluster cs=8 g=256 ept=32 vec"
+    assert osr.plan_describe(osr.OP_RMSNORM, 64, 32767, "bf16") == "cluster cs=8 g=256 ept=16 scalar"
     assert osr.plan_describe(osr.OP_SOFTMAX, 64, 152064, "bf16", "f32").startswith("staged cs=12")
 
 
@@ -238,7 +244,7 @@ def test_logsumexp_plans_and_validation(lib):
 
 def test_layernorm_plans_and_validation(lib):
     assert osr.plan_describe(osr.OP_LAYERNORM, 256, 5120, "f32") == "rows g=512 ept=16 vec"
-    assert osr.plan_describe(osr.OP_LAYERNORM, 4, 40000, "f32").startswith("cluster cs=3 g=1024")
+    assert osr.plan_describe(osr.OP_LAYERNORM, 4, 40000, "f32") == "cluster cs=10 g=256 ept=16 vec"
     assert osr.plan_describe(osr.OP_LAYERNORM, 2, 10 ** 6, "f32").startswith("split")
     f = ctypes.c_float(1e-5)
     assert lib.osr_layernorm_fwd(P, P * 8, None, f, P * 16, 4, 16, F32, None) == 1   # NULL beta
