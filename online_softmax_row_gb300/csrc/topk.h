@@ -27,6 +27,8 @@ struct TopkArgs {
 constexpr int kTopkThreads = 256;
 constexpr int64_t kTopkMaxK = 1024;
 constexpr int64_t kTopkMaxPieceBytes = 192 << 10;  // largest piece a CTA caches
+// the sweep keeps one bit per 16-byte vector of a thread in a 64-bit word
+static_assert(kTopkMaxPieceBytes / 16 / kTopkThreads <= 64, "vectors a thread sweeps");
 constexpr int kTopkMaxCluster = 16;
 constexpr int kTopkListCap = 1024;  // keys at or above a CTA's bound kept in a short list
 constexpr int64_t kTopkRankMaxK = 256;  // k up to this: outputs placed by counting, no sort
