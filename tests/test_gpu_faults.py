@@ -23,17 +23,22 @@ def gpu():
     osr.library()
 
 
-def test_wait_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("spec", ["staged:cs=2,r=0", "staged:cs=2,r=8"])
+def test_wait_timeout_is_reported_and_context_survives(spec):
+    # both shapes stage part of each piece in shared memory (with r=8 half of
+    # it is held in registers), so every CTA waits on its copies' barriers
     assert osr.device_fault() == 0
     x = workloads.softmax_inputs(1, 32768, "f32", sigma=2.0, seed=1)["x"].cuda()
-    assert osr.plan_describe(osr.OP_SOFTMAX, 1, 32768, "f32").startswith("staged")
     poison = torch.full((1, 32768), 0x7FC0DEAD, dtype=torch.int32, device="cuda")
     y = poison.view(torch.float32)
+    os.environ["OSR_FORCE_KERNEL"] = spec
     os.environ["OSR_TEST_HOOK"] = "no_arrive"
     try:
+        assert osr.plan_describe(osr.OP_SOFTMAX, 1, 32768, "f32").startswith("staged cs=2")
         osr.softmax_rows(x, out=y)
     finally:
         del os.environ["OSR_TEST_HOOK"]
+        del os.environ["OSR_FORCE_KERNEL"]
     assert osr.device_fault() == 1          # the bounded wait ran out and said so
     assert torch.all(poison == 0x7FC0DEAD)  # no stores after the failed wait
     assert osr.device_fault() == 0          # reading clears the word
