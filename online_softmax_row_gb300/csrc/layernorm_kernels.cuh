@@ -2,6 +2,8 @@
 // kernel and the two split-row passes.
 #pragma once
 
+#include <type_traits>
+
 #include "row_common.cuh"
 
 namespace osr {
@@ -64,7 +66,7 @@ layernorm_rows_kernel(const RowArgs a) {
             v[j] = t[0];
         }
     }
-    const uint64_t p2 = f2_make(p, p);
+    uint64_t p2 = f2_make(p, p);  // the pivot (bfloat16: moved near the mean for a second pass)
     // binary32 vectors: the pivot-shifted pairs are formed once and kept (the
     // same registers as the raw vectors; 4.30 -> 4.13 us on 256 x 5120).
     // bfloat16 vectors stay packed and are widened in each pass: keeping the
@@ -82,60 +84,138 @@ layernorm_rows_kernel(const RowArgs a) {
         else return f2_sub(f2_of<D>(q[j], k), p2);
     };
 
-    // sum of the pivot-shifted values
-    float s1 = 0.f;
-    if constexpr (kVec) {
-        uint64_t acc = f2_make(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < NU; ++j)
-            if (valid >> j & 1u) {
-#pragma unroll
-                for (int k = 0; k < PAIRS; ++k) acc = f2_add(acc, shifted2(j, k));
-            }
-        s1 = f2_lo(acc) + f2_hi(acc);
-    } else {
-#pragma unroll
-        for (int j = 0; j < NU; ++j)
-            if (valid >> j & 1u) s1 += v[j] - p;
-    }
+    // Statistics of the pivot-shifted values d = x - p.
+    // binary32 rows: the two-pass form, mu = sum(d)/H, then
+    // var = sum((d - mu)^2)/H.  A pivot hundreds of standard deviations from
+    // the mean costs them digits in x - p.
+    // bfloat16 rows: one pass for sum(d) and sum(d^2), reduced together,
+    // var = sum(d^2)/H - mu^2 (x - p is exact there: a difference of two
+    // 8-bit significands).  The subtraction loses log10(1 + mu^2/var)
+    // digits, so when mu^2 > 0.9 mean(d^2) (the pivot far from the mean) a
+    // second pass runs, the corrected two-pass algorithm (Chan, Golub &
+    // LeVeque, "Algorithms for computing the sample variance", 1983) about
+    // P = p + mu, a binary32 number next to the mean: with c = x - P,
+    // mu = sum(c)/H and var = sum(c^2)/H - mu^2, and the output offset is
+    // small as well.
+    constexpr bool kOnePass = kVec && D == Dt::BF16;
     __shared__ float red1[32], red2[32];
-    if constexpr (G <= 32) {
-        s1 = group_sum<G>(s1);
-    } else {
-        s1 = block_sum<RowsGeom<G>::kWarps>(s1, red1);
-    }
-    if constexpr (CLUSTER) s1 = cluster_sum(s1, a.cs, cluster_push_area<0>(), true);
-    const float mu = s1 / (float)a.N;  // mean of the shifted values
-    const uint64_t mu2 = f2_make(mu, mu);
-
-    // sum of squares about the mean
-    float s2 = 0.f;
+    float s1 = 0.f, q2 = 0.f;
     if constexpr (kVec) {
-        uint64_t acc = f2_make(0.f, 0.f);
+        uint64_t acc = f2_make(0.f, 0.f), acc2 = f2_make(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < NU; ++j)
             if (valid >> j & 1u) {
 #pragma unroll
                 for (int k = 0; k < PAIRS; ++k) {
-                    const uint64_t c = f2_sub(shifted2(j, k), mu2);
-                    acc = f2_fma(c, c, acc);
+                    const uint64_t d = shifted2(j, k);
+                    acc = f2_add(acc, d);
+                    if constexpr (kOnePass) acc2 = f2_fma(d, d, acc2);
                 }
             }
-        s2 = f2_lo(acc) + f2_hi(acc);
+        s1 = f2_lo(acc) + f2_hi(acc);
+        if constexpr (kOnePass) q2 = f2_lo(acc2) + f2_hi(acc2);
     } else {
 #pragma unroll
         for (int j = 0; j < NU; ++j)
-            if (valid >> j & 1u) {
-                const float c = (v[j] - p) - mu;
-                s2 = fmaf(c, c, s2);
+            if (valid >> j & 1u) s1 += v[j] - p;
+    }
+    // the row's sums of a and b: threads, warps (one shared-memory stage),
+    // cluster CTAs (exchange number X)
+    auto row_sums = [&](float &sa, float &sb, float *ra, float *rb, auto X) {
+        if constexpr (G <= 32) {
+            sa = group_sum<G>(sa);
+            sb = group_sum<G>(sb);
+        } else {
+            constexpr int NW = RowsGeom<G>::kWarps;
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            sa = group_sum<32>(sa);
+            sb = group_sum<32>(sb);
+            if (lane == 0) {
+                ra[warp] = sa;
+                rb[warp] = sb;
             }
-    }
-    if constexpr (G <= 32) {
-        s2 = group_sum<G>(s2);
+            __syncthreads();
+            sa = group_sum<NW>(ra[lane & (NW - 1)]);
+            sb = group_sum<NW>(rb[lane & (NW - 1)]);
+        }
+        if constexpr (CLUSTER) {
+            constexpr int ID = decltype(X)::value;
+            ClusterPush *x = cluster_push_area<ID>();
+            const bool got = cluster_push(x, make_uint4(__float_as_uint(sa), __float_as_uint(sb), 0u, 0u), a.cs, ID == 0);
+            const int lane = threadIdx.x & 31;
+            sa = group_sum<32>(lane < a.cs ? __uint_as_float(x->slot[lane].x) : 0.f);
+            sb = group_sum<32>(lane < a.cs ? __uint_as_float(x->slot[lane].y) : 0.f);
+            if (!got) sa = __int_as_float(0x7fffffff);
+        }
+    };
+    if constexpr (kOnePass) {
+        row_sums(s1, q2, red1, red2, std::integral_constant<int, 0>());
     } else {
-        s2 = block_sum<RowsGeom<G>::kWarps>(s2, red2);
+        if constexpr (G <= 32) {
+            s1 = group_sum<G>(s1);
+        } else {
+            s1 = block_sum<RowsGeom<G>::kWarps>(s1, red1);
+        }
+        if constexpr (CLUSTER) s1 = cluster_sum(s1, a.cs, cluster_push_area<0>(), true);
     }
-    if constexpr (CLUSTER) s2 = cluster_sum(s2, a.cs, cluster_push_area<1>(), false);
+    float mu = s1 / (float)a.N;  // mean of the shifted values
+    float s2 = 0.f;
+    bool second = true;
+    if constexpr (kOnePass) {
+        const float e2 = q2 / (float)a.N;  // mean of d^2 = var + mu^2
+        second = mu * mu > 0.9f * e2;      // the same in every thread and CTA of the row
+        s2 = fmaxf(e2 - mu * mu, 0.f) * (float)a.N;
+    }
+    if (second) {
+        if constexpr (kOnePass) {
+            p2 = f2_make(p + mu, p + mu);  // shifted2 now gives x - P
+            mu = 0.f;
+        }
+        const uint64_t m1 = f2_make(mu, mu);
+        float t1 = 0.f, t2 = 0.f;
+        if constexpr (kVec) {
+            uint64_t acc = f2_make(0.f, 0.f), acc2 = f2_make(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < NU; ++j)
+                if (valid >> j & 1u) {
+#pragma unroll
+                    for (int k = 0; k < PAIRS; ++k) {
+                        const uint64_t c = f2_sub(shifted2(j, k), m1);
+                        if constexpr (kOnePass) acc = f2_add(acc, c);
+                        acc2 = f2_fma(c, c, acc2);
+                    }
+                }
+            t1 = f2_lo(acc) + f2_hi(acc);
+            t2 = f2_lo(acc2) + f2_hi(acc2);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NU; ++j)
+                if (valid >> j & 1u) {
+                    const float c = (v[j] - p) - mu;
+                    t2 = fmaf(c, c, t2);
+                }
+        }
+        if constexpr (kOnePass) {
+            // second stage arrays: a warp may still read the first ones
+            __shared__ float red3[32], red4[32];
+            row_sums(t1, t2, red3, red4, std::integral_constant<int, 1>());
+            const float dm = t1 / (float)a.N;  // the mean of x - P
+            mu += dm;
+            s2 = fmaxf(t2 - t1 * dm, 0.f);
+        } else {
+            // binary32: the sum of squares about mu1 (the correction of mu1
+            // is below the rounding of x - p there, and cost 7 % on
+            // 256 x 5120)
+            if constexpr (G <= 32) {
+                t2 = group_sum<G>(t2);
+            } else {
+                t2 = block_sum<RowsGeom<G>::kWarps>(t2, red2);
+            }
+            if constexpr (CLUSTER) t2 = cluster_sum(t2, a.cs, cluster_push_area<1>(), false);
+            s2 = t2;
+        }
+    }
+    const uint64_t mu2 = f2_make(mu, mu);
     const float r = rsqrtf(s2 / (float)a.N + a.eps);
     const uint64_t r2 = f2_make(r, r);
 

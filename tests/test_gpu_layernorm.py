@@ -161,3 +161,21 @@ def test_layernorm_on_pinned_host_rows():
     dy = osr.layernorm_fwd(inp["x"].cuda(), inp["gamma"].cuda(), inp["beta"].cuda(), 1e-5)
     torch.cuda.synchronize()
     assert torch.equal(hy, dy.cpu())
+
+
+@pytest.mark.parametrize("H", [4096, 5120, 65536])
+def test_layernorm_bf16_one_pass_and_far_pivot(H):
+    # bf16 rows take their statistics in one pass about the pivot x[row][0];
+    # a pivot far from the mean (rows 0-1: x[0] = +-300 in N(0,1) rows) or an
+    # offset mean (rows 2-3: N(100, 1), N(-1000, 4)) loses digits there, and
+    # the exact second pass about the mean must take over
+    x, gamma, beta = ln_case(6, H, "f32", seed_of("ln-pivot", H))
+    x = x.float()
+    x[0, 0] = 300.0
+    x[1, 0] = -300.0
+    x[2] = x[2] + 100.0
+    x[3] = x[3] * 4.0 - 1000.0
+    xb, gb, bb = x.to(torch.bfloat16), gamma.to(torch.bfloat16), beta.to(torch.bfloat16)
+    y = osr.layernorm_fwd(xb.cuda(), gb.cuda(), bb.cuda(), EPS)
+    torch.cuda.synchronize()
+    check_ln(xb, gb, bb, y.cpu())
