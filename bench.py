@@ -13,8 +13,10 @@ row-length sweep), one dispatcher leaf each.
 
 Inputs are resident in HBM; consecutive steps rotate over enough distinct
 input/output sets that no step finds its data in L2 (more than twice the L2
-capacity of traffic between two uses of a set).  Device time comes from CUDA
-events on the launching stream around the K timed steps.
+capacity of traffic between two uses of a set).  The K timed steps are
+captured once in a CUDA graph before the timed region (`--stream-launches`:
+issued one by one instead); device time comes from CUDA events on the
+launching stream around one replay.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (rows are independent: weak scaling, no collective on the data path); the
@@ -305,13 +307,29 @@ def time_graph(osr, w, steps, warmup, device, l2_bytes):
     return ms, steps
 
 
-def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, sustain_s=0.0):
-    """Device time of `steps` back-to-back calls (rotating input sets)."""
+def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, sustain_s=0.0,
+                  graph=True, replay_warm=True):
+    """Device time of `steps` back-to-back calls (rotating input sets).
+    graph: the `steps` calls are captured once in a CUDA graph (outside the
+    timed region; launches with programmatic dependent launch become
+    programmatic edges) and the timed region is one replay of it, so host
+    launch gaps do not count; otherwise they are issued one by one."""
     sets = make_sets(w, n_sets_for(w, l2_bytes), device)
     stream = torch.cuda.current_stream(device)
     for i in range(max(warmup, 3)):
         call(osr, w, sets[i % len(sets)])
     torch.cuda.synchronize(device)
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                for i in range(steps):
+                    call(osr, w, sets[i % len(sets)])
+        if replay_warm:
+            g.replay()
+        torch.cuda.synchronize(device)
     sampler = ClockSampler(sampler_index) if sampler_index is not None else None
     clocks = None
 
@@ -336,8 +354,11 @@ def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, s
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for i in range(steps):
-            call(osr, w, sets[i % len(sets)])
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(steps):
+                call(osr, w, sets[i % len(sets)])
         stop.record(stream)
         torch.cuda.synchronize(device)
         elapsed_ms = start.elapsed_time(stop)
@@ -346,7 +367,7 @@ def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, s
         if sampler:
             sampler.__exit__(None, None, None)
             clocks = sampler.summary()
-    del sets
+    del g, sets
     torch.cuda.empty_cache()
     return elapsed_ms, clocks
 
@@ -520,7 +541,8 @@ def ours(args):
 
     elapsed_ms, clocks = time_workload(osr, w, args.steps, args.warmup, device, l2,
                                        sampler_index=None if args.profile else device.index,
-                                       sustain_s=0.0 if args.profile else 1.5)
+                                       sustain_s=0.0 if args.profile else 1.5,
+                                       graph=not args.stream_launches, replay_warm=not args.profile)
     max_ms, total_bytes = aggregate_over_ranks(elapsed_ms, w.min_bytes * args.steps, world)
     value = total_bytes / (max_ms * 1e-3) / 1e9
     per_launch_ms = elapsed_ms / args.steps / launches_per_call(plan, w.M)
@@ -536,6 +558,9 @@ def ours(args):
         "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
                    "out_dtype": w.out_dtype, "min_bytes_per_step": w.min_bytes, "kernel": plan,
                    "rows_capped": bool(args.max_rows and w.M == args.max_rows),
+                   "timing": ("the steps issued one by one on the stream" if args.stream_launches else
+                              "CUDA graph of the steps (programmatic dependent launch edges), captured "
+                              "before the timed region; CUDA events around one replay"),
                    "l2": f"rotating {n_sets_for(w, l2)} input/output sets (> 2x L2 of traffic "
                          f"between reuses); no flush", "parallelism": f"rows; {world} GPU(s), weak"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -619,6 +644,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-suite", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--stream-launches", action="store_true",
+                    help="time the steps launched one by one instead of one graph replay")
     ap.add_argument("--profile", action="store_true",
                     help="only the timed steps of the workload (for ncu captures): no clock "
                          "sampling, per-workload table, e2e or CPU baseline")
