@@ -26,6 +26,13 @@ constexpr int64_t kNoIndex = 0x7fffffffffffffffLL;
 constexpr int kLseEpt = 32;
 constexpr int kLseStagedHeader = 128;  // the copies' mbarrier, padded
 
+// per half: the larger number (a NaN loses to a number)
+__device__ __forceinline__ uint32_t lse_max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 template <int W>
 __device__ __forceinline__ int64_t group_min_i64(int64_t v) {
 #pragma unroll
@@ -75,41 +82,103 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
     pdl_wait();
 
     MaxArgSum t{-FLT_MAX, 0.f, kNoIndex};
-    if (s.ok) {
-        for (int64_t base = s.u0; base < s.u1; base += (int64_t)G * NU) {
-            float v[NU][U];
+    if constexpr (U > 1) {
+        // 16-byte vectors kept raw: the tile's maximum on packed pairs
+        // (max.bf16x2; a NaN loses, as with fmaxf), its exps on f32x2 pairs,
+        // and the element index searched only when the running maximum
+        // grows (a thread visits its elements in increasing index order, so
+        // an equal maximum later never moves the first index)
+        if (s.ok) {
+            const uint64_t l2e = f2_make(1.4426950408889634f, 1.4426950408889634f);
+            const uint32_t neg_inf = DI == Dt::BF16 ? 0xff80ff80u : 0xff800000u;
+            for (int64_t base = s.u0; base < s.u1; base += (int64_t)G * NU) {
+                uint4 q[NU];
 #pragma unroll
-            for (int j = 0; j < NU; ++j) {
-                const int64_t ui = base + (int64_t)j * G + s.t;
-                if (ui < s.u1) {
-                    load_unit<DI, U>(xrow, ui * U, v[j]);
+                for (int j = 0; j < NU; ++j) {
+                    const int64_t ui = base + (int64_t)j * G + s.t;
+                    q[j] = ui < s.u1 ? ld16<Hint::Stream>(xrow + ui * 16) : make_uint4(neg_inf, neg_inf, neg_inf, neg_inf);
+                }
+                float tm = -FLT_MAX;
+#pragma unroll
+                for (int j = 0; j < NU; ++j) {
+                    if constexpr (DI == Dt::BF16) {
+                        const uint32_t w = lse_max_bf16x2(lse_max_bf16x2(q[j].x, q[j].y), lse_max_bf16x2(q[j].z, q[j].w));
+                        tm = fmaxf(tm, fmaxf(bf16_lo(w), bf16_hi(w)));
+                    } else {
+                        tm = fmaxf(fmaxf(tm, fmaxf(__uint_as_float(q[j].x), __uint_as_float(q[j].y))),
+                                   fmaxf(__uint_as_float(q[j].z), __uint_as_float(q[j].w)));
+                    }
+                }
+                const uint64_t tm2 = f2_make(tm, tm);
+                uint64_t acc = f2_make(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NU; ++j)
+#pragma unroll
+                    for (int k = 0; k < U / 2; ++k) {
+                        const uint64_t e = f2_mul(f2_sub(f2_of<DI>(q[j], k), tm2), l2e);
+                        acc = f2_add(acc, f2_make(ex2_approx(f2_lo(e)), ex2_approx(f2_hi(e))));
+                    }
+                const float td = f2_lo(acc) + f2_hi(acc);
+                if (tm > t.m) {
+                    int64_t ti = kNoIndex;
+#pragma unroll
+                    for (int j = NU - 1; j >= 0; --j)
+#pragma unroll
+                        for (int k = U - 1; k >= 0; --k) {
+                            float v;
+                            if constexpr (DI == Dt::BF16) {
+                                const uint32_t w = k < 2 ? q[j].x : k < 4 ? q[j].y : k < 6 ? q[j].z : q[j].w;
+                                v = (k & 1) ? bf16_hi(w) : bf16_lo(w);
+                            } else {
+                                v = __uint_as_float(k == 0 ? q[j].x : k == 1 ? q[j].y : k == 2 ? q[j].z : q[j].w);
+                            }
+                            if (v == tm) ti = (base + (int64_t)j * G + s.t) * U + k;  // the last hit is the first
+                        }
+                    t.d = t.d * expf(t.m - tm) + td;
+                    t.m = tm;
+                    t.i = ti;
                 } else {
-#pragma unroll
-                    for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
+                    t.d += td * expf(tm - t.m);
                 }
             }
-            float tm = -FLT_MAX;
-            int64_t ti = kNoIndex;
+        }
+    } else {
+        if (s.ok) {
+            for (int64_t base = s.u0; base < s.u1; base += (int64_t)G * NU) {
+                float v[NU][U];
 #pragma unroll
-            for (int j = 0; j < NU; ++j)
+                for (int j = 0; j < NU; ++j) {
+                    const int64_t ui = base + (int64_t)j * G + s.t;
+                    if (ui < s.u1) {
+                        load_unit<DI, U>(xrow, ui * U, v[j]);
+                    } else {
 #pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (v[j][k] > tm) {
-                        tm = v[j][k];
-                        ti = (base + (int64_t)j * G + s.t) * U + k;
+                        for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
                     }
-            float td = 0.f;
+                }
+                float tm = -FLT_MAX;
+                int64_t ti = kNoIndex;
 #pragma unroll
-            for (int j = 0; j < NU; ++j)
+                for (int j = 0; j < NU; ++j)
 #pragma unroll
-                for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], tm);
-            if (tm > t.m) {
-                t.d = t.d * expf(t.m - tm) + td;
-                t.m = tm;
-                t.i = ti;
-            } else {
-                t.d += td * expf(tm - t.m);
-                if (tm == t.m && ti < t.i) t.i = ti;
+                    for (int k = 0; k < U; ++k)
+                        if (v[j][k] > tm) {
+                            tm = v[j][k];
+                            ti = (base + (int64_t)j * G + s.t) * U + k;
+                        }
+                float td = 0.f;
+#pragma unroll
+                for (int j = 0; j < NU; ++j)
+#pragma unroll
+                    for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], tm);
+                if (tm > t.m) {
+                    t.d = t.d * expf(t.m - tm) + td;
+                    t.m = tm;
+                    t.i = ti;
+                } else {
+                    t.d += td * expf(tm - t.m);
+                    if (tm == t.m && ti < t.i) t.i = ti;
+                }
             }
         }
     }
@@ -318,7 +387,8 @@ cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cu
     }
 #define OSR_MAKE(G) \
     if (g == G) fn = lse_argmax_kernel<DI, G, U, false>;
-    OSR_MAKE(1) OSR_MAKE(2) OSR_MAKE(4) OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(256)
+    OSR_MAKE(1) OSR_MAKE(2) OSR_MAKE(4) OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(64)
+    OSR_MAKE(128) OSR_MAKE(256)
 #undef OSR_MAKE
     if (!fn) return cudaErrorInvalidConfiguration;
     return launch_fn(fn, grid, g <= 32 ? RowsGeom<1>::kThreads : g, 0, a, st);

@@ -101,7 +101,8 @@ def test_log_softmax_minus_inf():
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N", [(1, 1), (7, 2), (100, 32), (33, 1000), (3, 1023), (64, 4096),
-                                 (9, 32768), (4, 152064), (1, 152064), (2, 300000), (300, 5000)])
+                                 (16, 2048), (9, 32768), (4, 152064), (1, 152064), (2, 300000),
+                                 (300, 5000)])
 def test_row_logsumexp(M, N, dt):
     x = case(M, N, dt, seed_of("lse", M, N, dt))
     lse, am = osr.row_logsumexp(x.cuda())
