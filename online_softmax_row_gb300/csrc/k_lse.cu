@@ -288,20 +288,35 @@ __global__ void __launch_bounds__(256) lse_staged_kernel(const RowArgs a) {
     if (!ok) mbar_wait_bounded(bar, 0, 1000000000ull);  // own copies still landing
 
     // the CTA's maximum and the first index holding it (each thread visits
-    // its elements in increasing index order; NaN never wins), then its sum
+    // its vectors in increasing index order and keeps the first vector whose
+    // maximum beats its running one; NaN never wins), then its sum of exps
+    // on f32x2 pairs
     float tm = -FLT_MAX;
-    int64_t ti = kNoIndex;
+    int ju = -1;  // the vector holding this thread's maximum
     if (ok) {
         for (int u = threadIdx.x; u < n; u += T) {
-            float v[U];
-            load_unit<DI, U, Hint::Keep>(stage, (int64_t)u * U, v);
-#pragma unroll
-            for (int k = 0; k < U; ++k)
-                if (v[k] > tm) {
-                    tm = v[k];
-                    ti = (u0 + u) * U + k;
-                }
+            const uint4 q = *reinterpret_cast<const uint4 *>(stage + u * 16);
+            float um;
+            if constexpr (DI == Dt::BF16) {
+                const uint32_t w = lse_max_bf16x2(lse_max_bf16x2(q.x, q.y), lse_max_bf16x2(q.z, q.w));
+                um = fmaxf(bf16_lo(w), bf16_hi(w));
+            } else {
+                um = fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                           fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+            }
+            if (um > tm) {
+                tm = um;
+                ju = u;
+            }
         }
+    }
+    int64_t ti = kNoIndex;
+    if (ju >= 0) {
+        float v[U];
+        load_unit<DI, U, Hint::Keep>(stage, (int64_t)ju * U, v);
+#pragma unroll
+        for (int k = U - 1; k >= 0; --k)
+            if (v[k] == tm) ti = (u0 + ju) * U + k;  // the last hit is the first
     }
     float m = group_max<32>(tm);
     if (lane == 0) s_m[warp] = m;
@@ -310,12 +325,17 @@ __global__ void __launch_bounds__(256) lse_staged_kernel(const RowArgs a) {
     const int64_t wi = group_min_i64<32>(tm == m ? ti : kNoIndex);
     float td = 0.f;
     if (ok) {
+        const uint64_t m2 = f2_make(m, m), l2e = f2_make(1.4426950408889634f, 1.4426950408889634f);
+        uint64_t acc = f2_make(0.f, 0.f);
         for (int u = threadIdx.x; u < n; u += T) {
-            float v[U];
-            load_unit<DI, U, Hint::Keep>(stage, (int64_t)u * U, v);
+            const uint4 q = *reinterpret_cast<const uint4 *>(stage + u * 16);
 #pragma unroll
-            for (int k = 0; k < U; ++k) td += exp_shifted(v[k], m);
+            for (int k = 0; k < U / 2; ++k) {
+                const uint64_t e = f2_mul(f2_sub(f2_of<DI>(q, k), m2), l2e);
+                acc = f2_add(acc, f2_make(ex2_approx(f2_lo(e)), ex2_approx(f2_hi(e))));
+            }
         }
+        td = f2_lo(acc) + f2_hi(acc);
     }
     const float wd = group_sum<32>(td);
     if (lane == 0) {
