@@ -142,11 +142,15 @@ osr_status osr_softmax_rows_stats(const void *x, void *y, float *row_max, float 
                                   void *stream);
 
 /*
- * Device-side fault report.  The staged softmax tier (rows longer than 16384
- * elements) waits for its bulk copies into shared memory with a bounded wait
- * (1 s); if a wait ever runs out, the kernel records the fault in a device
- * word, skips its stores and exits normally, so the context stays usable.
- * This call synchronises `stream`, copies that word to *fault (0 = none),
+ * Device-side fault report.  The staged softmax tier (16-byte rows longer
+ * than one CTA holds) waits for its bulk copies into shared memory (bound:
+ * 1 s) and for the other CTAs' (m, d) states (bound: 2 s); if a wait ever
+ * runs out, the kernel records the fault in a device word (bit 0: copies,
+ * bit 1: states), skips its stores and exits normally, so the context stays
+ * usable.  The other cluster kernels (the register cluster tier of every
+ * row op, log-sum-exp, top-k) bound their state exchanges the same way and
+ * report a time-out in their outputs instead: NaN values, -1 indices.
+ * This call synchronises `stream`, copies the word to *fault (0 = none),
  * clears it, and returns OSR_ERR_DEVICE_TIMEOUT if it was set, OSR_OK if not
  * (OSR_ERR_INVALID for a NULL fault pointer, OSR_ERR_CUDA on a CUDA error).
  * The word is per device and shared by all streams of the process.
