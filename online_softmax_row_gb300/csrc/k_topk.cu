@@ -85,11 +85,6 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
 __device__ __forceinline__ uint64_t ld_dsmem_u64(uint32_t addr) {
     uint64_t v;
     asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr));
@@ -242,7 +237,6 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
     __shared__ uint32_t s_scan[kWarps];
     __shared__ float s_ez[kTopkRankMaxK];
     __shared__ uint32_t pub_cand, list_n, s_bin, s_krem;
-    __shared__ uint32_t s_off[kTopkMaxCluster + 1];
     __shared__ uint64_t s_top;
     // exchanges without a cluster barrier: st.async into the receiver's
     // shared memory, counted on its mbarrier.  xbar[0]: every CTA's
