@@ -343,22 +343,31 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     int64_t cs = 1;
     const char *force = getenv("OSR_FORCE_KERNEL");
     int64_t fcs = 0;
+    const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
+    // staged: 12 CTAs per row (16 for one or two rows), each piece
+    // bulk-copied whole, when the grid fits one wave (shared memory allows
+    // CTAs an SM by the piece).  Measured on 152064-element rows: staged was
+    // 11-26 % faster than streaming while it fit one wave (bf16 up to 96
+    // rows, fp32 up to 48: 32 bf16 rows 7.1 -> 5.3 us, 64 bf16 rows 8.6 ->
+    // 7.7 us) and up to 20 % slower beyond (64 fp32 rows: 10.4 -> 11.3 us).
+    bool staged_fit = false;
+    int64_t cs_st = M <= 2 ? 16 : 12;
+    if (cs_st > most) cs_st = most;
+    if (vec && cs_st > 1) {
+        const int64_t smem = 128 + cdiv(nunits, cs_st) * 16;
+        const int64_t per_sm = (int64_t)(228 << 10) / (smem + 1024);  // 1 KiB reserved a CTA
+        const int64_t slots = (per_sm < 8 ? per_sm : 8) * sms;
+        staged_fit = smem <= kStagedMaxSmem && M * cs_st <= slots;
+    }
     if (force && strncmp(force, "lse", 3) == 0 && parse_kv(force, "cs", &fcs) && fcs >= 1 && fcs <= 16) {
         cs = fcs;  // a forced cluster size (tests)
-    } else if (M <= 16 && vec && 128 + cdiv(nunits, M <= 2 ? 16 : 12) * 16 <= kStagedMaxSmem) {
-        // up to 16 rows of 16-byte units: staged pieces (below), 16 CTAs per
-        // row for one or two rows, 12 otherwise (measured on 152064-element
-        // bf16 rows: 1 row 3.83 -> 3.19 us, 8 rows 4.11 -> 3.77 us against
-        // the best streaming cluster)
-        cs = M <= 2 ? 16 : 12;
-        const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
-        if (cs > most) cs = most;
-        if (cs < 1) cs = 1;
+    } else if (staged_fit) {
+        cs = cs_st;
     } else if (M < 2 * (int64_t)sms) {
-        // measured on 152064-element rows: 10 CTAs per row for up to 16 rows
-        // (18 % faster than 8), 4 for more (8 % faster than 8 at 64 rows)
+        // streaming clusters, measured on 152064-element rows: 10 CTAs per
+        // row for up to 16 rows (18 % faster than 8), 4 for more (8 % faster
+        // than 8 at 64 rows)
         cs = M <= 16 ? 10 : 4;
-        const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
         if (cs > most) cs = most;
         if (cs < 1) cs = 1;
     }
@@ -366,9 +375,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     lp.cs = (int)cs;
     lp.chunk = cdiv(nunits, cs);
     lp.grid = M * cs;
-    // few rows of 16-byte units: each piece staged whole in shared memory
-    // (streaming was as fast or faster from 64 rows on)
-    int64_t st = M <= 16 ? 1 : 0;
+    int64_t st = staged_fit ? 1 : 0;
     if (force && strncmp(force, "lse", 3) == 0) parse_kv(force, "st", &st);
     if (cs > 1 && vec && st != 0 && 128 + lp.chunk * 16 <= kStagedMaxSmem) {
         lp.staged = true;

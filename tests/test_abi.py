@@ -225,7 +225,13 @@ def test_forced_kernel(monkeypatch):
 
 
 def test_logsumexp_plans_and_validation(lib):
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
+    # staged while 12 CTAs a row fit one wave (bf16 pieces 25 KiB: 8 an SM;
+    # fp32 pieces 50 KiB: 4 an SM), streaming clusters of 4 beyond
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 96, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 128, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "f32") == "lse-cluster g=256 cs=4 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 1, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32", vec_ok=False) == "lse-cluster g=256 cs=10 scalar"
@@ -266,8 +272,10 @@ def test_topk_plans_and_validation(lib, monkeypatch):
         D(osr.OP_TOPK, 1, 786433, "f32")                                        # beyond 16 x 192 KiB
     monkeypatch.setenv("OSR_FORCE_KERNEL", "topk:cs=8")
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=8 piece=38016B vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16,st=0")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=16 vec"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     monkeypatch.delenv("OSR_FORCE_KERNEL")
     T = lib.osr_row_topk
     assert T(P, P * 8, P * 16, None, None, 0, 16, 4, F32, None) == 0            # M == 0
