@@ -242,8 +242,9 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
     // shared memory, counted on its mbarrier.  xbar[0]: every CTA's
     // (m, d, list length) into xstate[its rank] of every CTA; xbar[1]: on
     // the short path, every CTA's list into CTA 0's union
-    __shared__ __align__(8) uint64_t xbar_words[2];
+    __shared__ __align__(8) uint64_t xbar_words[3];
     __shared__ uint4 xstate[kTopkMaxCluster];
+    __shared__ float2 xg[kTopkMaxCluster];  // xbar[2]: every CTA's bound g
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cs = a.cs;
@@ -280,13 +281,16 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         }
     };
 
-    const uint32_t xbar0 = smem_u32(&xbar_words[0]), xbar1 = smem_u32(&xbar_words[1]);
+    const uint32_t xbar0 = smem_u32(&xbar_words[0]), xbar1 = smem_u32(&xbar_words[1]),
+                   xbar2 = smem_u32(&xbar_words[2]);
     if (tid == 0) {
         pub_cand = 0;
         list_n = 0;
         mbar_init(xbar0, 1);
         mbar_init(xbar1, 1);
+        mbar_init(xbar2, 1);
         mbar_arrive_expect_tx(xbar0, (uint32_t)cs * 16u);
+        mbar_arrive_expect_tx(xbar2, (uint32_t)cs * 8u);
         fence_mbar_init();
     }
     __syncthreads();
@@ -341,6 +345,18 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         for (int w = 0; w < kWarps; ++w) g = fminf(g, s_gw[w]);
     }
 
+    // Every CTA's g is a lower bound of the row's k-th largest (it holds k
+    // elements >= g), so their maximum is one too: sent to every CTA now,
+    // read after the exps, so the lists keep only elements >= that maximum.
+    cluster_wait_acquire();  // every peer's barriers are initialised
+    if (tid < cs) st_async_f2(mapa_shared(smem_u32(&xg[rank]), tid), mapa_shared(xbar2, tid), g, 0.f);
+    auto row_bound = [&]() {
+        float gr = g;
+        if (mbar_wait_bounded(xbar2, 0, 2000000000ull))  // else the exchange below fails
+            for (int r = 0; r < cs; ++r) gr = fmaxf(gr, xg[r].x);
+        return gr;
+    };
+
     // ---- one sweep: this CTA's (m, d) for the log-sum-exp, and the elements
     //      not below g, as (key, column) words, into a short list
     const float mc = fmaxf(cmax, -FLT_MAX);
@@ -380,6 +396,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
             hit |= (uint64_t)!(um < g) << j;
         }
         const float d0 = f2_lo(acc), d1 = f2_hi(acc);
+        const float gr = row_bound();
         while (hit != 0) {
             const int j = __ffsll((long long)hit) - 1;
             hit &= hit - 1;
@@ -387,13 +404,14 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
             const uint4 q = pv[i];
 #pragma unroll
             for (int e = 0; e < U; ++e)
-                if (!(raw_value_at<DI>(q, e) < g)) keep(raw_bits_at<DI>(q, e), e0 + (int64_t)i * U + e);
+                if (!(raw_value_at<DI>(q, e) < gr)) keep(raw_bits_at<DI>(q, e), e0 + (int64_t)i * U + e);
         }
         dt = d0 + d1;
     } else {
+        const float gr = row_bound();
         sweep_piece([&](float v, uint32_t bits, int64_t col) {
             dt += exp_shifted(v, mc);
-            if (!(v < g)) keep(bits, col);
+            if (!(v < gr)) keep(bits, col);
         });
     }
     dt = block_sum_f(dt, s_red);  // also orders the list appends
@@ -401,7 +419,6 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
 
     // ---- exchange: the row's (m, d) by the merge of the CTAs' (m, d), and
     //      the lists' lengths
-    cluster_wait_acquire();  // every peer's barriers are initialised
     if (tid < cs)
         st_async_v4(mapa_shared(smem_u32(&xstate[rank]), tid), mapa_shared(xbar0, tid),
                     make_uint4(__float_as_uint(mc), __float_as_uint(dt), nl, 0u));
