@@ -304,6 +304,19 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
             return OSR_OK;
         }
     }
+    // LayerNorm on up to 256 16-byte bf16 rows: one vector a thread, up to
+    // 512 threads (its two reductions and the pairs' arithmetic make each
+    // thread's chain long; measured 1.04-1.29x faster on 2048-8192-element
+    // rows, e.g. 64 x 2048: 2.84 -> 2.25 us).  RMSNorm and softmax measured
+    // the same either way.
+    if (op == Op::LayerNorm && vec && in_dt == OSR_BF16 && M <= 256 && g <= 512) {
+        const int gs = pow2ceil(nunits < 512 ? nunits : 512);
+        if (gs > g) {
+            p->tier = Tier::Rows;
+            p->g = gs;
+            return OSR_OK;
+        }
+    }
     if (g <= gmax && (g <= 512 || cs256 > max_cluster)) {
         p->tier = Tier::Rows;
         p->g = g;
