@@ -561,11 +561,12 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
         cs = fcs;
         tp->forced = true;
     } else {
-        // measured on 1-256 rows of 152064 elements: 12 CTAs per row for up to
-        // 16 rows (7-11 % faster than 16), 4 up to 96 rows (10 % faster than 8
-        // at 64), 6 beyond; never fewer than the row needs, and never so many
-        // that a CTA gets less than one vector per thread
-        const int64_t fill = M <= 16 ? 12 : M <= 96 ? 4 : 6;
+        // measured on 1-256 rows of 152064 elements: 8 CTAs per row for up to
+        // 16 rows (3-5 % faster than 12 with the row-wide bound, 7-11 %
+        // faster than 16), 4 up to 96 rows (10 % faster than 8 at 64), 6
+        // beyond; never fewer than the row needs, and never so many that a
+        // CTA gets less than one vector per thread
+        const int64_t fill = M <= 16 ? 8 : M <= 96 ? 4 : 6;
         if (fill > cs) cs = fill;
         while (cs > cs_min && cdiv(N, cs) < (int64_t)kTopkThreads * u) cs = cs / 2 > cs_min ? cs / 2 : cs_min;
     }

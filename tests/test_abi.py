@@ -262,7 +262,7 @@ def test_layernorm_plans_and_validation(lib):
 def test_topk_plans_and_validation(lib, monkeypatch):
     D = osr.plan_describe
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
-    assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=12 piece=25344B vec"   # few rows: 12 CTAs
+    assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=8 piece=38016B vec"    # few rows: 8 CTAs
     assert D(osr.OP_TOPK, 256, 152064, "bf16") == "topk cs=6 piece=50688B vec"
     assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=4 piece=152064B vec"
     assert D(osr.OP_TOPK, 8, 1000, "bf16") == "topk cs=1 piece=2000B vec"       # short rows: one CTA
