@@ -358,6 +358,8 @@ struct LsePlan {
     size_t smem = 0;      // staged: dynamic shared memory per CTA
 };
 
+constexpr int kSmemPerSm = 228 << 10;  // shared memory of an sm_100-family SM (1 KiB of it reserved a CTA)
+
 LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     LsePlan lp;
     const int u = vec ? vec_elems(in_dt) : 1;
@@ -388,7 +390,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     if (cs_st > most) cs_st = most;
     if (vec && cs_st > 1) {
         const int64_t smem = 128 + cdiv(nunits, cs_st) * 16;
-        const int64_t per_sm = (int64_t)(228 << 10) / (smem + 1024);  // 1 KiB reserved a CTA
+        const int64_t per_sm = (int64_t)kSmemPerSm / (smem + 1024);  // 1 KiB reserved a CTA
         const int64_t slots = (per_sm < 8 ? per_sm : 8) * sms;
         staged_fit = smem <= kStagedMaxSmem && M * cs_st <= slots;
     }
