@@ -54,7 +54,7 @@ __device__ __forceinline__ MaxArgSum group_mas(MaxArgSum t) {
     MaxArgSum r;
     r.m = group_max<W>(t.m);
     r.i = group_min_i64<W>(t.m == r.m ? t.i : kNoIndex);
-    r.d = group_sum<W>(t.d * expf(t.m - r.m));
+    r.d = group_sum<W>(t.d * md_factor(t.m, r.m));
     return r;
 }
 
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
     }
     pdl_wait();
 
-    MaxArgSum t{-FLT_MAX, 0.f, kNoIndex};
+    MaxArgSum t{-INFINITY, 0.f, kNoIndex};
     if constexpr (U > 1) {
         // 16-byte vectors kept raw: the tile's maximum on packed pairs
         // (max.bf16x2; a NaN loses, as with fmaxf), its exps on f32x2 pairs,
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
                     const int64_t ui = base + (int64_t)j * G + s.t;
                     q[j] = ui < s.u1 ? ld16<Hint::Stream>(xrow + ui * 16) : make_uint4(neg_inf, neg_inf, neg_inf, neg_inf);
                 }
-                float tm = -FLT_MAX;
+                float tm = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < NU; ++j) {
                     if constexpr (DI == Dt::BF16) {
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
                                    fmaxf(__uint_as_float(q[j].z), __uint_as_float(q[j].w)));
                     }
                 }
-                const uint64_t tm2 = f2_make(tm, tm);
+                const uint64_t tm2 = f2_make(md_shift(tm), md_shift(tm));
                 uint64_t acc = f2_make(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < NU; ++j)
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
                     t.m = tm;
                     t.i = ti;
                 } else {
-                    t.d += td * expf(tm - t.m);
+                    t.d += td * md_factor(tm, t.m);
                 }
             }
         }
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
                         for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
                     }
                 }
-                float tm = -FLT_MAX;
+                float tm = -INFINITY;
                 int64_t ti = kNoIndex;
 #pragma unroll
                 for (int j = 0; j < NU; ++j)
@@ -170,13 +170,13 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
 #pragma unroll
                 for (int j = 0; j < NU; ++j)
 #pragma unroll
-                    for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], tm);
+                    for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], md_shift(tm));
                 if (tm > t.m) {
                     t.d = t.d * expf(t.m - tm) + td;
                     t.m = tm;
                     t.i = ti;
                 } else {
-                    t.d += td * expf(tm - t.m);
+                    t.d += td * md_factor(tm, t.m);
                     if (tm == t.m && ti < t.i) t.i = ti;
                 }
             }
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
         __syncthreads();
         m = group_max<NW>(s_m[lane & (NW - 1)]);
         const int64_t wi = group_min_i64<32>(t.m == m ? t.i : kNoIndex);
-        const float wd = group_sum<32>(t.d * expf(t.m - m));
+        const float wd = group_sum<32>(t.d * md_factor(t.m, m));
         if (lane == 0) {
             s_d[warp] = wd;
             s_i[warp] = wi;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
         const bool got = mbar_wait_bounded(xbar, 0, 2000000000ull);
         // lanes q and q + 16 take CTA q's state, the same order in every CTA
         const int q = threadIdx.x & 15;
-        MaxArgSum p{-FLT_MAX, 0.f, kNoIndex};
+        MaxArgSum p{-INFINITY, 0.f, kNoIndex};
         if (q < a.cs) {
             const uint4 v = xslot[q];
             p = MaxArgSum{__uint_as_float(v.x), __uint_as_float(v.y),
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(256) lse_staged_kernel(const RowArgs a) {
     // its vectors in increasing index order and keeps the first vector whose
     // maximum beats its running one; NaN never wins), then its sum of exps
     // on f32x2 pairs
-    float tm = -FLT_MAX;
+    float tm = -INFINITY;
     int ju = -1;  // the vector holding this thread's maximum
     if (ok) {
         for (int u = threadIdx.x; u < n; u += T) {
@@ -325,7 +325,8 @@ __global__ void __launch_bounds__(256) lse_staged_kernel(const RowArgs a) {
     const int64_t wi = group_min_i64<32>(tm == m ? ti : kNoIndex);
     float td = 0.f;
     if (ok) {
-        const uint64_t m2 = f2_make(m, m), l2e = f2_make(1.4426950408889634f, 1.4426950408889634f);
+        const uint64_t m2 = f2_make(md_shift(m), md_shift(m)),
+                       l2e = f2_make(1.4426950408889634f, 1.4426950408889634f);
         uint64_t acc = f2_make(0.f, 0.f);
         for (int u = threadIdx.x; u < n; u += T) {
             const uint4 q = *reinterpret_cast<const uint4 *>(stage + u * 16);
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(256) lse_staged_kernel(const RowArgs a) {
     }
     ok = mbar_wait_bounded(xbar, 0, 2000000000ull) && ok;
     const int q = threadIdx.x & 15;
-    MaxArgSum p{-FLT_MAX, 0.f, kNoIndex};
+    MaxArgSum p{-INFINITY, 0.f, kNoIndex};
     if (q < a.cs) {
         const uint4 v = xslot[q];
         p = MaxArgSum{__uint_as_float(v.x), __uint_as_float(v.y), (int64_t)(((uint64_t)v.w << 32) | v.z)};

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(cons
         }
     }
     uint4 r[RU > 0 ? RU : 1];
-    float mt = -FLT_MAX, dt = 0.f;
+    float mt = -INFINITY, dt = 0.f;
 #pragma unroll
     for (int j = 0; j < RU; ++j)
         if (threadIdx.x + j * T < nr) r[j] = ld16<Hint::Stream>(src + (size_t)(threadIdx.x + j * T) * 16);
@@ -133,22 +133,23 @@ __global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(cons
 #pragma unroll
             for (int k = 0; k < U; ++k) mt = fmaxf(mt, v[k]);
         }
+        const float ms = md_shift(mt);
 #pragma unroll
         for (int j = 0; j < RU; ++j)
             if (threadIdx.x + j * T < nr) {
                 float v[U];
                 unit_values<DI>(r[j], v);
 #pragma unroll
-                for (int k = 0; k < U; ++k) dt += exp_shifted(v[k], mt);
+                for (int k = 0; k < U; ++k) dt += exp_shifted(v[k], ms);
             }
         for (int u = threadIdx.x; u < ns; u += T) {
             float v[U];
             lds_unit<DI>(stage + u * 16, v);
 #pragma unroll
-            for (int k = 0; k < U; ++k) dt += exp_shifted(v[k], mt);
+            for (int k = 0; k < U; ++k) dt += exp_shifted(v[k], ms);
         }
     } else {
-        mt = -FLT_MAX;
+        mt = -INFINITY;
         dt = 0.f;
     }
     __shared__ float red_m[32], red_d[32];
@@ -166,14 +167,14 @@ __global__ void __launch_bounds__(T, RU == 0 ? 1 : 4) softmax_staged_kernel(cons
         // lane r (and r + 16) takes CTA r's state: the same fixed order in
         // every CTA, so all pieces of a row scale by the same (m, d)
         const int from = threadIdx.x & 15;
-        float pm = -FLT_MAX, pd = 0.f;
+        float pm = -INFINITY, pd = 0.f;
         if (from < a.cs) {
             const float2 q = xslot[from];
             pm = q.x;
             pd = q.y;
         }
         rn.m = group_max<16>(pm);
-        rn.d = group_sum<16>(pd * expf(pm - rn.m));
+        rn.d = group_sum<16>(pd * md_factor(pm, rn.m));
     }
 
     if (ok) {

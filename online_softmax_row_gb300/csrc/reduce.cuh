@@ -6,11 +6,14 @@
 //   sum of squares (RMSNorm), identity 0;
 //   the online-softmax normaliser state (m, d) with the merge
 //     (m1, d1) (+) (m2, d2) = (max(m1, m2), d1 e^(m1 - m) + d2 e^(m2 - m)),
-//   identity (-inf, 0) -- represented as (-FLT_MAX, 0) so that merging two
-//   empty states never evaluates (-inf) - (-inf).
+//   identity (-inf, 0).  An empty state (m = -inf: no element, or only -inf
+//   and NaN elements) is never rescaled by e^(m_t - m): its factor is 0
+//   (a NaN in its d still propagates, 0 * NaN = NaN), so two empty states
+//   never evaluate (-inf) - (-inf), and a row of only -inf ends as
+//   (m, d) = (-inf, 0): its exact maximum and the empty sum.
 // Merge and identity: "两个融合算子：RMSNorm 与 online softmax"
 // (daleiyang.github.io), §5·三 "结合律：为什么能做树形归约" (associativity,
-// identity, the -FLT_MAX substitute) and §3·三 "联合归约：把 (m, s) 当成一个整体";
+// identity) and §3·三 "联合归约：把 (m, s) 当成一个整体";
 // "RMSNorm、Softmax 与在线归约" (notes.kuangjux.top), "从逐元素更新到合并两个 tile".
 //
 // Every exchange is an xor butterfly of an exactly commutative operation
@@ -29,7 +32,17 @@ struct MD {
     float m, d;
 };
 
-__device__ __forceinline__ MD md_identity() { return {-FLT_MAX, 0.f}; }
+__device__ __forceinline__ MD md_identity() { return {-INFINITY, 0.f}; }
+
+// e^(mt - m), the factor that rescales a state of maximum mt to the maximum
+// m >= mt; 0 for an empty state (mt = -inf), also when m = -inf.
+__device__ __forceinline__ float md_factor(float mt, float m) {
+    return mt == -INFINITY ? 0.f : expf(mt - m);
+}
+
+// The shift a thread's exps are taken against: its maximum, or 0 while it
+// has seen no number above -inf (its exps are then e^-inf = 0, or NaN).
+__device__ __forceinline__ float md_shift(float mt) { return mt == -INFINITY ? 0.f : mt; }
 
 // One exp per merge: the side with the larger m is scaled by e^0 = 1.
 __device__ __forceinline__ MD md_merge(MD a, MD b) {
@@ -38,7 +51,7 @@ __device__ __forceinline__ MD md_merge(MD a, MD b) {
         a = b;
         b = t;
     }
-    return {a.m, fmaf(b.d, expf(b.m - a.m), a.d)};
+    return {a.m, fmaf(b.d, md_factor(b.m, a.m), a.d)};
 }
 
 // ---------------------------------------------------------------- in a group
@@ -75,7 +88,7 @@ template <int W>
 __device__ __forceinline__ RowNorm group_norm(float mt, float dt) {
     RowNorm r;
     r.m = group_max<W>(mt);
-    r.f = expf(mt - r.m);
+    r.f = md_factor(mt, r.m);
     r.d = group_sum<W>(dt * r.f);
     return r;
 }
@@ -92,7 +105,7 @@ __device__ __forceinline__ RowNorm block_norm(float mt, float dt, float *red_m, 
         m = group_max<NW>(red_m[lane & (NW - 1)]);
     }
     r.m = m;
-    r.f = expf(mt - m);
+    r.f = md_factor(mt, m);
     float d = group_sum<32>(dt * r.f);
     if constexpr (NW > 1) {
         if (lane == 0) red_d[warp] = d;
@@ -162,16 +175,16 @@ __device__ __forceinline__ bool cluster_push(ClusterPush *x, uint4 v, int cs, bo
 __device__ __forceinline__ RowNorm cluster_norm(float mt, RowNorm c, int cs, ClusterPush *x, bool first) {
     const bool ok = cluster_push(x, make_uint4(__float_as_uint(c.m), __float_as_uint(c.d), 0u, 0u), cs, first);
     const int r = threadIdx.x & 15;
-    float pm = -FLT_MAX, pd = 0.f;
+    float pm = -INFINITY, pd = 0.f;
     if (r < cs) {
         pm = __uint_as_float(x->slot[r].x);
         pd = __uint_as_float(x->slot[r].y);
     }
     RowNorm out;
     out.m = group_max<16>(pm);
-    out.d = group_sum<16>(pd * expf(pm - out.m));
+    out.d = group_sum<16>(pd * md_factor(pm, out.m));
     if (!ok) out.d = __int_as_float(0x7fffffff);
-    out.f = expf(mt - out.m);
+    out.f = md_factor(mt, out.m);
     return out;
 }
 

@@ -35,19 +35,20 @@ softmax_rows_kernel(const RowArgs a) {
         }
     }
 
-    float mt = -FLT_MAX;
+    float mt = -INFINITY;
 #pragma unroll
     for (int j = 0; j < NU; ++j)
 #pragma unroll
         for (int k = 0; k < U; ++k) mt = fmaxf(mt, v[j][k]);
     // log-softmax keeps the inputs; softmax replaces them by their exps
     const bool logm = (a.flags & kFlagLog) != 0;
+    const float ms = md_shift(mt);
     float dt = 0.f;
 #pragma unroll
     for (int j = 0; j < NU; ++j)
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const float e = exp_shifted(v[j][k], mt);
+            const float e = exp_shifted(v[j][k], ms);
             dt += e;
             v[j][k] = logm ? v[j][k] : e;
         }
@@ -106,16 +107,17 @@ __global__ void __launch_bounds__(G) softmax_split_stats_kernel(const RowArgs a)
                 for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
             }
         }
-        float tm = -FLT_MAX;
+        float tm = -INFINITY;
 #pragma unroll
         for (int j = 0; j < NU; ++j)
 #pragma unroll
             for (int k = 0; k < U; ++k) tm = fmaxf(tm, v[j][k]);
+        const float ts = md_shift(tm);
         float td = 0.f;
 #pragma unroll
         for (int j = 0; j < NU; ++j)
 #pragma unroll
-            for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], tm);
+            for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], ts);
         st = md_merge(st, MD{tm, td});
     }
     __shared__ float red_m[32], red_d[32];
