@@ -222,7 +222,9 @@ int osr_last_cuda_error(void);
  *             3 = log-softmax, 4 = log-sum-exp / argmax, 5 = LayerNorm,
  *             6 = top-k (the geometry for k = 64; k sizes only the sort)
  *   vec_ok    1 if every buffer is 16-byte aligned (the 128-bit path)
- *   sm_count  streaming multiprocessors of the target device (152 on GB300)
+ *   sm_count  streaming multiprocessors of the target device (152 on GB300);
+ *             the plan assumes 228 KiB of shared memory per SM (GB300), where
+ *             the compute entry points read the current device's figure
  *   buf       receives a NUL-terminated description, e.g.
  *             "rows g=256 ept=16 vec" or "cluster cs=10 g=1024 ept=16 vec"
  * Honours the OSR_FORCE_KERNEL environment variable exactly as the
@@ -251,10 +253,17 @@ osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_
  * that array until the process exits.
  *   - M may be at most OSR_NOALLOC_MAX_PARTIALS; larger M returns
  *     OSR_ERR_UNSUPPORTED before any device work.  Rows are cut into fewer
- *     pieces when needed so that M x pieces fits the array.
+ *     pieces when needed so that M x pieces fits the array (only for very
+ *     large inputs: more than 32768 rows, each longer than 165 KB); each
+ *     launch then takes more rows, whose second read may partly miss L2.
+ *   - Buffers: device, managed or mapped page-locked host memory, exactly
+ *     as osr_softmax_rows accepts them.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: it does not survive cudaDeviceReset or a switch to another
+ *     primary context on that device, after which this call must not be
+ *     used.
  *   - All calls share the one array and it keeps whatever the last call
  *     wrote.  Nothing in it needs to start at zero: every slot a call reads
  *     is written earlier in the same call.  Calls whose work overlaps on the

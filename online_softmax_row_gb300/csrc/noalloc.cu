@@ -64,13 +64,17 @@ bool overlap(const void *a, int64_t an, const void *b, int64_t bn) {
     return pa < pb + bn && pb < pa + an;
 }
 
+// Memory the device reads and writes at the same address: device or managed
+// memory, or page-locked host memory mapped into the unified address space
+// (the kernels then reach it over the host link), as osr_softmax_rows takes.
 bool on_device(const void *p) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+    return at.type == cudaMemoryTypeHost && at.devicePointer == p;
 }
 
 cudaError_t launch_pass(osr_dtype in_dt, osr_dtype out_dt, Kind k, const RowArgs &a, bool vec,
@@ -125,7 +129,15 @@ extern "C" osr_status osr_softmax_rows_noalloc(const void *x, void *y, int64_t M
                          ((int64_t)osr::kSplitThreads * upt);
     if (S > most) S = most;
     if (S > osr::kMaxPieces) S = osr::kMaxPieces;
-    if (S > OSR_NOALLOC_MAX_PARTIALS / M) S = OSR_NOALLOC_MAX_PARTIALS / M;
+    if (S > OSR_NOALLOC_MAX_PARTIALS / M) {
+        // the array caps the pieces: take more rows per batch instead, so
+        // that each launch still has about two CTAs per SM (their re-read in
+        // pass 2 may then come partly from HBM rather than L2)
+        S = OSR_NOALLOC_MAX_PARTIALS / M;
+        if (S < 1) S = 1;
+        const int64_t fill = (2ll * sms + S - 1) / S;
+        if (b < fill) b = fill < M ? fill : M;
+    }
     if (S > nunits) S = nunits;
     if (S < 1) S = 1;
 
