@@ -11,6 +11,7 @@
 // passes through a small global workspace.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <stdio.h>
@@ -19,6 +20,7 @@
 #include <string.h>
 
 #include "../../include/osr.h"
+#include "../../include/osr_test.h"
 #include "launch.h"
 #include "staged.h"
 #include "topk.h"
@@ -27,6 +29,9 @@ namespace osr {
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+
+// osr_test_set_flags (include/osr_test.h): read once per staged launch
+std::atomic<int> g_test_flags{0};
 
 osr_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
@@ -54,9 +59,14 @@ int pow2ceil(int64_t v) {
 }
 
 // ------------------------------------------------------------ device facts
+// shared memory of an sm_100-family SM (1 KiB of it is reserved per CTA):
+// the planners' default where no device is queried (osr_plan_describe)
+constexpr int kSmemPerSmDefault = 228 << 10;
+
 struct DeviceInfo {
     int sms = 0;
     int max_cluster = 8;
+    int smem_per_sm = kSmemPerSmDefault;
 };
 
 osr_status device_info(DeviceInfo *out) {
@@ -76,6 +86,9 @@ osr_status device_info(DeviceInfo *out) {
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
             return cuda_fail(e);
         if ((e = cudaDeviceGetAttribute(&cluster, cudaDevAttrClusterLaunch, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess)
             return cuda_fail(e);
         d.max_cluster = cluster ? (major >= 10 ? 16 : 8) : 1;
         cache[dev] = d;
@@ -358,9 +371,7 @@ struct LsePlan {
     size_t smem = 0;      // staged: dynamic shared memory per CTA
 };
 
-constexpr int kSmemPerSm = 228 << 10;  // shared memory of an sm_100-family SM (1 KiB of it reserved a CTA)
-
-LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
+LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int smem_per_sm) {
     LsePlan lp;
     const int u = vec ? vec_elems(in_dt) : 1;
     const int64_t nunits = vec ? N / u : N;
@@ -390,7 +401,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms) {
     if (cs_st > most) cs_st = most;
     if (vec && cs_st > 1) {
         const int64_t smem = 128 + cdiv(nunits, cs_st) * 16;
-        const int64_t per_sm = (int64_t)kSmemPerSm / (smem + 1024);  // 1 KiB reserved a CTA
+        const int64_t per_sm = (int64_t)smem_per_sm / (smem + 1024);  // 1 KiB reserved a CTA
         const int64_t slots = (per_sm < 8 ? per_sm : 8) * sms;
         staged_fit = smem <= kStagedMaxSmem && M * cs_st <= slots;
     }
@@ -614,8 +625,7 @@ osr_status execute(Op op, osr_dtype in_dt, osr_dtype out_dt, RowArgs a, const Pl
         if (grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
         a.cs = p.cs;
         a.chunk = p.chunk;
-        const char *hook = getenv("OSR_TEST_HOOK");
-        if (hook && strcmp(hook, "no_arrive") == 0) a.flags |= kFlagNoArrive;
+        if (g_test_flags.load(std::memory_order_relaxed) & OSR_TEST_NO_ARRIVE) a.flags |= kFlagNoArrive;
         if (in_dt == OSR_F32 && out_dt == OSR_F32)
             e = launch_softmax_staged<Dt::F32, Dt::F32>(a, grid, p.smem, p.g, p.ru, st);
         else if (in_dt == OSR_F32 && out_dt == OSR_BF16)
@@ -708,6 +718,8 @@ const char *osr_status_string(osr_status s) {
 
 int osr_last_cuda_error(void) { return g_last_cuda_error; }
 
+int osr_test_set_flags(int flags) { return g_test_flags.exchange(flags); }
+
 int osr_version(void) { return 100; }
 
 osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
@@ -729,7 +741,7 @@ osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_
     if (s != OSR_OK) return s;
     const bool vec = vec_ok && (N % vec_elems(in_dt)) == 0;
     if (op == 4) {
-        const LsePlan lp = lse_plan(M, N, in_dt, vec, sm_count);
+        const LsePlan lp = lse_plan(M, N, in_dt, vec, sm_count, kSmemPerSmDefault);
         if (lp.staged)
             snprintf(buf, buf_len, "lse-staged g=%d cs=%d piece=%lldB %s", lp.g, lp.cs,
                      (long long)lp.chunk * 16, vec ? "vec" : "scalar");
@@ -908,7 +920,7 @@ osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t
     DeviceInfo di;
     if ((s = device_info(&di)) != OSR_OK) return s;
     const bool vec = aligned16(x) && N % vec_elems(in_dt) == 0;
-    const LsePlan lp = lse_plan(M, N, in_dt, vec, di.sms);
+    const LsePlan lp = lse_plan(M, N, in_dt, vec, di.sms, di.smem_per_sm);
     if (lp.grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
     RowArgs a = {};
     a.x = x;

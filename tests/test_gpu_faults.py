@@ -1,10 +1,12 @@
 """Bounded device waits report a fault instead of hanging.
 
 The staged softmax tier waits for its bulk copies into shared memory with a
-1 s bound.  A test hook (OSR_TEST_HOOK=no_arrive) makes that barrier receive
-no arrival -- a flag nothing sets -- so the wait runs out: the kernel must
+1 s bound.  A test-only entry point (osr_test_set_flags with
+OSR_TEST_NO_ARRIVE, include/osr_test.h) makes that barrier receive no
+arrival -- a flag nothing sets -- so the wait runs out: the kernel must
 record the fault, skip its stores, leave the cluster cleanly, and the
 context must keep working.  Nothing here faults, traps or hangs the GPU."""
+import ctypes
 import os
 
 import pytest
@@ -14,6 +16,14 @@ import online_softmax_row_gb300 as osr
 import workloads
 
 pytestmark = pytest.mark.gpu
+NO_ARRIVE = 1  # OSR_TEST_NO_ARRIVE in include/osr_test.h
+
+
+def set_test_flags(flags: int) -> int:
+    fn = osr.library().osr_test_set_flags
+    fn.argtypes = [ctypes.c_int]
+    fn.restype = ctypes.c_int
+    return fn(flags)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -32,12 +42,12 @@ def test_wait_timeout_is_reported_and_context_survives(spec):
     poison = torch.full((1, 32768), 0x7FC0DEAD, dtype=torch.int32, device="cuda")
     y = poison.view(torch.float32)
     os.environ["OSR_FORCE_KERNEL"] = spec
-    os.environ["OSR_TEST_HOOK"] = "no_arrive"
+    assert set_test_flags(NO_ARRIVE) == 0
     try:
         assert osr.plan_describe(osr.OP_SOFTMAX, 1, 32768, "f32").startswith("staged cs=2")
         osr.softmax_rows(x, out=y)
     finally:
-        del os.environ["OSR_TEST_HOOK"]
+        assert set_test_flags(0) == NO_ARRIVE
         del os.environ["OSR_FORCE_KERNEL"]
     assert osr.device_fault() == 1          # the bounded wait ran out and said so
     assert torch.all(poison == 0x7FC0DEAD)  # no stores after the failed wait
