@@ -278,9 +278,11 @@ def launches_per_call(plan: str, M: int) -> int:
     return 1
 
 
-def time_graph(osr, w, steps, warmup, device, l2_bytes):
-    """Device time of `steps` calls captured once in a CUDA graph and replayed
-    (rotating input sets): the kernels' own time without host launch cost."""
+def time_graph(osr, w, steps, warmup, device, l2_bytes, replays=21):
+    """Device time of `steps` calls captured once in a CUDA graph (rotating
+    input sets), replayed `replays` times: the kernels' own time without host
+    launch cost.  Returns the per-call milliseconds of every replay (CUDA
+    events on the launching stream around each replay) and the step count."""
     sets = make_sets(w, n_sets_for(w, l2_bytes), device)
     steps = max(steps, len(sets))  # every set once: no call finds its inputs in L2
     for i in range(max(warmup, 3)):
@@ -294,17 +296,36 @@ def time_graph(osr, w, steps, warmup, device, l2_bytes):
                 call(osr, w, sets[i % len(sets)])
     g.replay()
     torch.cuda.synchronize(device)
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
     cur = torch.cuda.current_stream(device)
-    start.record(cur)
-    g.replay()
-    stop.record(cur)
-    torch.cuda.synchronize(device)
-    ms = start.elapsed_time(stop)
+    per_call = []
+    for _ in range(replays):
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(cur)
+        g.replay()
+        stop.record(cur)
+        torch.cuda.synchronize(device)
+        per_call.append(start.elapsed_time(stop) / steps)
     del g, sets
     torch.cuda.empty_cache()
-    return ms, steps
+    return per_call, steps
+
+
+def quantile(v, q):
+    """The q-quantile of v (linear between order statistics)."""
+    v = sorted(v)
+    pos = q * (len(v) - 1)
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (pos - lo)
+
+
+# The five configurations of the metric: C1 RMSNorm fp32, C2 fused bf16,
+# C3 attention softmax fp32, C4 vocabulary softmax bf16 -> fp32, C5 the
+# fp32 row-length sweep
+BASELINE_CONFIGS = [("C1", "rmsnorm_f32_64x3584"), ("C2", "fused_add_rmsnorm_bf16_8192x4096"),
+                    ("C3", "softmax_attn_f32_114688x4096"), ("C4", "softmax_vocab_bf16_f32_64x152064")] + \
+    [(f"C5 N={n}", f"softmax_sweep_f32_N{n}") for n in (32, 128, 1024, 4096, 32768, 152064)]
 
 
 def time_workload(osr, w, steps, warmup, device, l2_bytes, sampler_index=None, sustain_s=0.0,
@@ -457,23 +478,48 @@ def copy_peak(osr, device, gib=2):
     return 2 * n / (best * 1e-3) / 1e9
 
 
-def cpu_baseline_for(w, budget_s=8.0):
-    """The oracle, as it stands (single thread), on a bounded sample of rows of
-    the same workload; value in the workload's GB/s (min bytes of the sample)."""
-    import oracle
-    oracle.set_threads(1)
-    rows = w.M
-    # estimate with a small probe, then size the sample to about budget_s
-    probe = max(1, min(rows, 4096 // max(1, w.N // 1024) or 1))
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+    if m:
+        return m.group(1).strip()
+    m = re.search(r"^CPU part\s*:\s*(\S+)$", info, re.M)  # Arm: the part number
+    if m:
+        part = m.group(1).lower()
+        return {"0xd4f": "Arm Neoverse V2"}.get(part, f"Arm CPU part {part}")
+    return "unknown"
+
+
+def _oracle_sample(oracle, w, threads, budget_s):
+    """Time the oracle with `threads` threads on about budget_s of rows."""
+    oracle.set_threads(threads)
+    probe = max(1, min(w.M, 4096 // max(1, w.N // 1024) or 1))
     t = _oracle_time(oracle, w, probe)
     per_row = max(t / probe, 1e-7)
-    sample = int(max(1, min(rows, budget_s / per_row)))
+    sample = int(max(1, min(w.M, budget_s / per_row)))
     t = _oracle_time(oracle, w, sample)
-    frac = sample / w.M
-    gbs = w.min_bytes * frac / t / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.get_threads(), "kind": "oracle",
-            "sample": f"{sample} of {w.M} rows of {w.name} (seed 0), fp64 C oracle, {t:.2f} s",
-            "seconds": round(t, 3)}
+    return sample, t, w.min_bytes * sample / w.M / t / 1e9
+
+
+def cpu_baseline_for(w, budget_s=6.0):
+    """The oracle, as it stands, on a bounded sample of rows of the same
+    workload: on every host core (OpenMP over rows) and on one; value in the
+    workload's GB/s (min bytes of the sample)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    sample, t, gbs = _oracle_sample(oracle, w, cores, budget_s)
+    s1, t1, gbs1 = _oracle_sample(oracle, w, 1, budget_s)
+    oracle.set_threads(1)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{sample} of {w.M} rows of {w.name} (seed 0), fp64 C oracle, {cores} threads, "
+                      f"{t:.2f} s",
+            "seconds": round(t, 3), "nproc": cores, "cpu_model": cpu_model(),
+            "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{s1} of {w.M} rows, {t1:.2f} s"}}
 
 
 def _oracle_inputs(w, rows):
@@ -574,25 +620,44 @@ def ours(args):
     if rank == 0 and not (args.no_suite or args.profile):
         result["peaks"] = {"nominal_gbs": NOMINAL_HBM_GBS, "driver_measured_gbs": peak,
                            "copy_kernel_same_run_gbs": round(copy_peak(osr, device), 1)}
+        copy_gbs = result["peaks"]["copy_kernel_same_run_gbs"]
         suite = []
         for name, wl in workloads.WORKLOADS.items():
             steps = max(20, min(2000, int(1e10 / max(wl.min_bytes, 1))))
-            ms, steps = time_graph(osr, wl, steps, 5, device, l2)
+            per_call, steps = time_graph(osr, wl, steps, 5, device, l2)
             p = osr.plan_describe(OP_CODE[wl.op], wl.M, wl.N, wl.in_dtype, wl.out_dtype, True,
                                   props.multi_processor_count)
-            g = wl.min_bytes * steps / (ms * 1e-3) / 1e9
+            us = [t * 1e3 for t in per_call]
+            med = statistics.median(us)
+            g = wl.min_bytes / (med * 1e-6) / 1e9
             suite.append({"workload": name, "kernel": p, "min_bytes": wl.min_bytes, "steps": steps,
-                          "timing": "CUDA graph of the steps, CUDA events around one replay",
-                          "us_per_call": round(ms / steps * 1e3, 3), "gbs": round(g, 1),
+                          "us_per_call": round(med, 3), "us_p10": round(quantile(us, 0.1), 3),
+                          "us_p90": round(quantile(us, 0.9), 3), "replays": len(us), "gbs": round(g, 1),
                           "frac_measured": round(g / peak, 4), "frac_nominal": round(g / NOMINAL_HBM_GBS, 4),
-                          "frac_copy_same_run": round(g / result["peaks"]["copy_kernel_same_run_gbs"], 4),
+                          "frac_copy_same_run": round(g / copy_gbs, 4),
                           "launches_per_call": launches_per_call(p, wl.M),
                           "traffic": profiled_traffic(wl, p)})
         result["per_kernel"] = suite
+        result["per_kernel_timing"] = ("per workload: CUDA graph of the steps over rotating sets, "
+                                       "replayed 21 times with CUDA events around each replay; "
+                                       "median and p10/p90 of the per-call time")
+        by_name = {e["workload"]: e for e in suite}
+        baseline_configs = {}
+        for tag, name in BASELINE_CONFIGS:
+            e = by_name[name]
+            baseline_configs[tag] = {"us": e["us_per_call"], "p10": e["us_p10"], "p90": e["us_p90"],
+                                     "gbs": e["gbs"], "frac": e["frac_measured"],
+                                     "frac_copy": e["frac_copy_same_run"], "traffic": e["traffic"]}
     if rank == 0:
         if not args.profile:
             result["e2e"] = time_e2e(osr, w, max(3, min(args.steps, 50)), args.warmup, device)
             result["cpu_baseline"] = cpu_baseline_for(w)
+        if not (args.no_suite or args.profile):
+            # last, and compact, so that a reader keeping only the end of the
+            # line still sees every configuration of the metric: median us
+            # over 21 graph replays, p10/p90, GB/s, fraction of the measured
+            # peak and of the copy kernel in this run, ncu DRAM bytes
+            result["baseline_configs"] = baseline_configs
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -607,10 +672,11 @@ def reference(args):
         return
     import oracle
     oracle.build()
-    oracle.set_threads(1)
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)  # OpenMP over rows, every host core
     w = workloads.WORKLOADS[args.workload]
     # each step: a bounded sample of rows of the same workload
-    rows = max(1, min(w.M, int(2_000_000 // max(w.N, 1))))
+    rows = max(1, min(w.M, int(8_000_000 // max(w.N, 1))))
     inp = _oracle_inputs(w, rows)
     for _ in range(max(args.warmup, 0)):
         _run_oracle(oracle, w, inp)
@@ -620,7 +686,7 @@ def reference(args):
     dt = time.perf_counter() - t0
     sample_bytes = w.min_bytes * rows / w.M
     value = sample_bytes * args.steps / dt / 1e9
-    sample = f"{rows} of {w.M} rows of {w.name} per step (seed 0), fp64 C oracle"
+    sample = f"{rows} of {w.M} rows of {w.name} per step (seed 0), fp64 C oracle, {cores} threads"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -629,7 +695,7 @@ def reference(args):
         "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
                    "out_dtype": w.out_dtype, "sample_rows_per_step": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.get_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "nproc": cores, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

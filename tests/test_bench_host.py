@@ -39,3 +39,22 @@ def test_traffic_applies_only_to_the_same_sources_and_plan(tmp_path, monkeypatch
     assert bench.profiled_traffic(w, "rows g=256 ept=16 vec") == 480_000_000
     assert bench.profiled_traffic(w, "rows g=128 ept=16 vec") is None   # stale sources
     assert bench.profiled_traffic(w, "rows g=512 ept=16 vec") is None   # other plan
+
+
+def test_quantiles_and_the_metric_configurations():
+    v = [float(i) for i in range(21)]
+    assert bench.quantile(v, 0.5) == 10.0
+    assert bench.quantile(v, 0.1) == 2.0 and bench.quantile(v, 0.9) == 18.0
+    assert bench.quantile([3.0, 1.0], 0.5) == 2.0
+    # every configuration of the metric is a workload the suite times
+    assert len(bench.BASELINE_CONFIGS) == 10
+    for tag, name in bench.BASELINE_CONFIGS:
+        assert name in workloads.WORKLOADS, (tag, name)
+
+
+def test_cpu_baseline_reports_all_cores_and_one(monkeypatch):
+    w = workloads.WORKLOADS["rmsnorm_f32_64x3584"]
+    cb = bench.cpu_baseline_for(w, budget_s=0.05)
+    assert cb["cores"] == (os.cpu_count() or 1) and cb["nproc"] == cb["cores"]
+    assert cb["single_thread"]["cores"] == 1 and cb["value"] > 0 and cb["single_thread"]["value"] > 0
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
