@@ -29,6 +29,11 @@ rmsnorm_rows_kernel(const RowArgs a) {
     if constexpr (CLUSTER) cluster_push_init(cluster_push_area<0>(), nullptr, a.cs);
     pdl_wait();
 
+    // The residual stores come after every load of the thread's units: the
+    // pointers are not known to be distinct, so a load placed after a store
+    // could not be moved ahead of it, and each unit would cost its own memory
+    // round trip.
+    char *rrow = reinterpret_cast<char *>(a.res) + row_off;
     uint4 pk[NP], gp[NP];
     float v[NF][U], g[NF][U];
 #pragma unroll
@@ -40,7 +45,6 @@ rmsnorm_rows_kernel(const RowArgs a) {
             if (in) {
                 pk[j] = ld16<Hint::Stream>(xrow + ui * 16);
                 if constexpr (FUSED) {
-                    char *rrow = reinterpret_cast<char *>(a.res) + row_off;
                     const uint4 rq = ld16<Hint::Stream>(rrow + ui * 16);
                     float xf[8], rf[8];
                     unpack8(pk[j], xf);
@@ -48,23 +52,32 @@ rmsnorm_rows_kernel(const RowArgs a) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) xf[k] += rf[k];
                     pk[j] = pack8(xf);
-                    __stcs(reinterpret_cast<uint4 *>(rrow + ui * 16), pk[j]);
                 }
             }
         } else {
             if (in) {
                 load_unit<D, U>(xrow, ui * U, v[j]);
                 if constexpr (FUSED) {
-                    char *rrow = reinterpret_cast<char *>(a.res) + row_off;
                     float r[U];
                     load_unit<D, U>(rrow, ui * U, r);
 #pragma unroll
                     for (int k = 0; k < U; ++k) v[j][k] = round_to<D>(v[j][k] + r[k]);
-                    store_unit<D, U>(rrow, ui * U, v[j]);
                 }
             } else {
 #pragma unroll
                 for (int k = 0; k < U; ++k) v[j][k] = 0.f;
+            }
+        }
+    }
+    if constexpr (FUSED) {
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = s.u0 + (int64_t)j * G + s.t;
+            if (s.ok && ui < s.u1) {
+                if constexpr (kPacked)
+                    __stcs(reinterpret_cast<uint4 *>(rrow + ui * 16), pk[j]);
+                else
+                    store_unit<D, U>(rrow, ui * U, v[j]);
             }
         }
     }
