@@ -5,8 +5,11 @@ z = ((x - p) - mu_s) * r; the summation trees for mu_s and var put a relative
 error of a few 1e-6 into z, and the final addition of beta can cancel, so the
 error is bounded by the size of the terms, not of the result:
   binary32 out: |gpu - ref| <= 1e-6 + 1e-5 (|z gamma| + |beta|)
-  bf16 out:     |gpu - ref| <= one bf16 ulp of ref + 1e-5 (|z gamma| + |beta|)
-with z, gamma, beta from the oracle's statistics (fp64)."""
+  bf16 out:     |gpu - ref| <= one bf16 ulp of ref + 1e-6 + 1e-5 (|z gamma| + |beta|)
+with z, gamma, beta from the oracle's statistics (fp64).  The 1e-6 is the
+binary32 arithmetic's absolute floor for both output types: the mean's
+summation tree rounds at the scale of sum(x - p), and an output that cancels
+to near zero (z gamma = -beta, both small) keeps that absolute error."""
 import os
 
 import numpy as np
@@ -58,7 +61,7 @@ def check_ln(x, gamma, beta, y):
         bound = 1e-6 + 1e-5 * scale
     else:
         ulp = np.where(ref != 0, 2.0 ** (np.floor(np.log2(np.abs(ref) + 1e-300)) - 7), 2.0 ** -133)
-        bound = ulp + 1e-5 * scale
+        bound = ulp + 1e-6 + 1e-5 * scale
     bad = ~(np.abs(got - ref) <= bound)
     if bad.any():
         i = tuple(np.argwhere(bad)[0])
