@@ -50,7 +50,9 @@
  *   (cudaMallocAsync / cudaFreeAsync on `stream`).
  * - M == 0 is a no-op returning OSR_OK.  Row length <= 0, M < 0, a NULL
  *   required pointer, or a dtype value outside osr_dtype return
- *   OSR_ERR_INVALID before any device work.  Errors are reported only by
+ *   OSR_ERR_INVALID before any device work.  M and the row length may each
+ *   be up to 2^40 and their product up to 2^59; beyond that the call returns
+ *   OSR_ERR_UNSUPPORTED before any device work.  Errors are reported only by
  *   return value: nothing is printed and the process is never terminated.
  * - Entry points are thread-safe; calls on the same stream execute in order.
  */

@@ -693,6 +693,8 @@ bool device_accessible(const void *p) {
 osr_status check_sizes(int64_t M, int64_t N) {
     if (M < 0 || N <= 0) return OSR_ERR_INVALID;
     if (N > ((int64_t)1 << 40) || M > ((int64_t)1 << 40)) return OSR_ERR_UNSUPPORTED;
+    // byte sizes (M x N x up to 8 bytes) must fit int64 arithmetic
+    if (M > 0 && N > ((int64_t)1 << 59) / M) return OSR_ERR_UNSUPPORTED;
     return OSR_OK;
 }
 

@@ -66,6 +66,10 @@ def test_invalid_sizes_and_dtypes(lib):
     assert lib.osr_softmax_rows(None, P, 1, 4, F32, F32, None) == 1        # NULL x
     assert lib.osr_rmsnorm_fwd(P, None, ctypes.c_float(0), P * 4, 1, 4, F32, None) == 1
     assert lib.osr_fused_add_rmsnorm(P, None, P * 2, ctypes.c_float(0), P * 4, 1, 4, F32, None) == 1
+    # sizes whose byte counts would not fit int64: refused before anything else
+    assert lib.osr_softmax_rows(P, P * 4, 2 ** 30, 2 ** 30, F32, F32, None) == 4
+    assert lib.osr_rmsnorm_fwd(P, P, ctypes.c_float(0), P * 4, 2 ** 40, 2 ** 20, F32, None) == 4
+    assert lib.osr_softmax_rows(P, P * 4, 1, 2 ** 41, F32, F32, None) == 4
 
 
 def test_alias_rules(lib):
