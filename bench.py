@@ -460,26 +460,56 @@ def time_e2e(osr, w, steps, warmup, device):
                     "write the outputs to host memory over NVLink-C2C (no staging copy)"}
 
 
-def copy_peak(osr, device, gib=2):
+def copy_peak(osr, device, gib=2, copy=None):
+    """Best of 10 device-to-device copies of `gib` GiB (read + write bytes
+    over time), by the library's copy kernel or the runtime's memcpy."""
+    copy = copy or osr.bench_copy
     n = gib * (1 << 30)
     a = torch.empty(n, dtype=torch.uint8, device=device)
     b = torch.empty(n, dtype=torch.uint8, device=device)
     a.fill_(1)
     for _ in range(3):
-        osr.bench_copy(a, b)
+        copy(a, b)
     torch.cuda.synchronize(device)
     best = float("inf")
     for _ in range(10):
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record()
-        osr.bench_copy(a, b)
+        copy(a, b)
         e.record()
         torch.cuda.synchronize(device)
         best = min(best, s.elapsed_time(e))
     del a, b
     torch.cuda.empty_cache()
     return 2 * n / (best * 1e-3) / 1e9
+
+
+def time_single_calls(osr, w, device, l2_bytes, calls=21):
+    """Device-side latency of one call issued alone: CUDA events around each
+    of `calls` stream launches on rotating input sets (cold in L2),
+    synchronised between calls.  A short GPU spin is queued before each start
+    event, so that the host has enqueued the call by the time the GPU reaches
+    the event and the figure is the device's, not the host's launch cost;
+    returns the per-call microseconds."""
+    sets = make_sets(w, n_sets_for(w, l2_bytes), device)
+    for i in range(3):
+        call(osr, w, sets[i % len(sets)])
+    torch.cuda.synchronize(device)
+    cur = torch.cuda.current_stream(device)
+    us = []
+    for i in range(calls):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)  # about 0.1 ms of GPU spin ahead of the timed call
+        s.record(cur)
+        call(osr, w, sets[(i + 3) % len(sets)])
+        e.record(cur)
+        torch.cuda.synchronize(device)
+        us.append(s.elapsed_time(e) * 1e3)
+    del sets
+    torch.cuda.empty_cache()
+    return us
 
 
 def cpu_model() -> str:
@@ -641,9 +671,12 @@ def ours(args):
     if sustained is not None:
         result["sustained"] = sustained
     if rank == 0 and not (args.no_suite or args.profile):
+        ck = copy_peak(osr, device)
+        mc = copy_peak(osr, device, copy=osr.bench_memcpy)
         result["peaks"] = {"nominal_gbs": NOMINAL_HBM_GBS, "driver_measured_gbs": peak,
-                           "copy_kernel_same_run_gbs": round(copy_peak(osr, device), 1)}
-        copy_gbs = result["peaks"]["copy_kernel_same_run_gbs"]
+                           "copy_kernel_same_run_gbs": round(ck, 1), "memcpy_d2d_same_run_gbs": round(mc, 1),
+                           "copy_max_same_run_gbs": round(max(ck, mc), 1)}
+        copy_gbs = result["peaks"]["copy_max_same_run_gbs"]
         suite = []
         for name, wl in workloads.WORKLOADS.items():
             steps = max(20, min(2000, int(1e10 / max(wl.min_bytes, 1))))
@@ -660,6 +693,10 @@ def ours(args):
                           "frac_copy_same_run": round(g / copy_gbs, 4),
                           "launches_per_call": launches_per_call(p, wl.M),
                           "traffic": profiled_traffic(wl, p)})
+            if wl.min_bytes < (64 << 20):
+                # small calls are latency-bound: one call issued alone as well
+                lat = time_single_calls(osr, wl, device, l2)
+                suite[-1]["latency_us"] = round(statistics.median(lat), 3)
         result["per_kernel"] = suite
         result["per_kernel_timing"] = ("per workload: CUDA graph of the steps over rotating sets, "
                                        "replayed 21 times with CUDA events around each replay; "
@@ -671,6 +708,8 @@ def ours(args):
             baseline_configs[tag] = {"us": e["us_per_call"], "p10": e["us_p10"], "p90": e["us_p90"],
                                      "gbs": e["gbs"], "frac": e["frac_measured"],
                                      "frac_copy": e["frac_copy_same_run"], "traffic": e["traffic"]}
+            if "latency_us" in e:
+                baseline_configs[tag]["latency_us"] = e["latency_us"]
     if rank == 0:
         if not args.profile:
             result["e2e"] = time_e2e(osr, w, max(3, min(args.steps, 50)), args.warmup, device)

@@ -1,7 +1,8 @@
 /*
  * osr_bench.h -- measurement helpers that ship with the library but are not
- * part of the row-wise path: a 128-bit device-to-device copy used to measure
- * the achievable HBM bandwidth in the same run as the row kernels.
+ * part of the row-wise path: a 128-bit device-to-device copy kernel and the
+ * runtime's device-to-device memcpy, used to measure the achievable HBM
+ * bandwidth in the same run as the row kernels.
  */
 #ifndef OSR_BENCH_H
 #define OSR_BENCH_H
@@ -24,6 +25,14 @@ extern "C" {
  * failure.  Asynchronous on `stream`.
  */
 osr_status osr_bench_copy(const void *src, void *dst, size_t bytes, void *stream);
+
+/*
+ * dst[0, bytes) <- src[0, bytes) by the runtime's cudaMemcpyAsync
+ * (device to device): a second reading of the achievable copy bandwidth,
+ * beside the copy kernel above.  Same arguments and errors as
+ * osr_bench_copy; any size and alignment.  Asynchronous on `stream`.
+ */
+osr_status osr_bench_memcpy(const void *src, void *dst, size_t bytes, void *stream);
 
 #ifdef __cplusplus
 }

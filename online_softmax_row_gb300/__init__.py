@@ -19,6 +19,7 @@ row_logsumexp        osr_row_logsumexp
 row_topk             osr_row_topk
 plan_describe        osr_plan_describe
 bench_copy           osr_bench_copy
+bench_memcpy         osr_bench_memcpy
 device_fault         osr_device_fault
 """
 from __future__ import annotations
@@ -34,7 +35,7 @@ from . import build as _build
 __all__ = ["OsrError", "rmsnorm_fwd", "layernorm_fwd", "OP_LAYERNORM", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
            "log_softmax_rows", "row_logsumexp", "row_topk", "OP_LOG_SOFTMAX", "OP_LOGSUMEXP",
            "OP_TOPK",
-           "plan_describe", "bench_copy", "device_fault", "library", "library_path", "OP_RMSNORM",
+           "plan_describe", "bench_copy", "bench_memcpy", "device_fault", "library", "library_path", "OP_RMSNORM",
            "OP_FUSED",
            "OP_SOFTMAX"]
 
@@ -81,13 +82,14 @@ def library():
         lib.osr_plan_describe.argtypes = [I, I64, I64, I, I, I, I, ctypes.c_char_p, ctypes.c_size_t]
         lib.osr_version.restype = I
         lib.osr_bench_copy.argtypes = [P, P, ctypes.c_size_t, P]
+        lib.osr_bench_memcpy.argtypes = [P, P, ctypes.c_size_t, P]
         lib.osr_device_fault.argtypes = [P, ctypes.POINTER(I)]
         lib.osr_log_softmax_rows.argtypes = [P, P, I64, I64, I, I, P]
         lib.osr_layernorm_fwd.argtypes = [P, P, P, F, P, I64, I64, I, P]
         lib.osr_row_logsumexp.argtypes = [P, P, P, I64, I64, I, P]
         lib.osr_row_topk.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
         for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
-                   "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy",
+                   "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy", "osr_bench_memcpy",
                    "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp", "osr_row_topk",
                    "osr_layernorm_fwd"):
             getattr(lib, fn).restype = I
@@ -290,6 +292,15 @@ def bench_copy(src: torch.Tensor, dst: torch.Tensor) -> None:
         raise OsrError(1, "bench_copy", "sizes differ")
     _check(_run(src, library().osr_bench_copy, src.data_ptr(), dst.data_ptr(), nbytes),
            "osr_bench_copy")
+
+
+def bench_memcpy(src: torch.Tensor, dst: torch.Tensor) -> None:
+    """dst <- src bytes by the runtime's device-to-device memcpy (HBM peak probe)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise OsrError(1, "bench_memcpy", "sizes differ")
+    _check(_run(src, library().osr_bench_memcpy, src.data_ptr(), dst.data_ptr(), nbytes),
+           "osr_bench_memcpy")
 
 
 def device_fault(device=None) -> int:

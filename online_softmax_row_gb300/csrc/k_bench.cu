@@ -1,4 +1,5 @@
-// k_bench.cu -- 128-bit copy kernel for the measured HBM peak (include/osr_bench.h).
+// k_bench.cu -- 128-bit copy kernel and device-to-device memcpy for the
+// measured HBM peak (include/osr_bench.h).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,4 +38,16 @@ extern "C" osr_status osr_bench_copy(const void *src, void *dst, size_t bytes, v
     copy16_kernel<<<4 * sms, 512, 0, (cudaStream_t)stream>>>((const uint4 *)src, (uint4 *)dst,
                                                               (int64_t)(bytes / 16));
     return cudaGetLastError() == cudaSuccess ? OSR_OK : OSR_ERR_CUDA;
+}
+
+extern "C" osr_status osr_bench_memcpy(const void *src, void *dst, size_t bytes, void *stream) {
+    if (bytes == 0) return OSR_OK;
+    if (!src || !dst) return OSR_ERR_INVALID;
+    const char *s = (const char *)src, *d = (const char *)dst;
+    if (s < d + bytes && d < s + bytes) return OSR_ERR_ALIAS;
+    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return OSR_ERR_CUDA;
+    }
+    return OSR_OK;
 }
