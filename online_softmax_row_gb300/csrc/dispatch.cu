@@ -358,10 +358,11 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
 
 // Log-sum-exp / argmax geometry: the kernel streams, so any shape fits; it
 // only has to spread the rows.  Short rows: a group of g <= 32 lanes per row.
-// Otherwise one 256-thread CTA per row, and when there are fewer rows than
-// two per SM, a cluster of CTAs per row (sizes below; 16-CTA clusters were
-// 70 % slower on 64 vocabulary rows).  OSR_FORCE_KERNEL="lse:cs=<n>" picks
-// the cluster size (tests).
+// Otherwise one CTA per row, or a cluster of CTAs per row while there are
+// too few rows to fill the GPU (sizes below; 16-CTA clusters were 70 %
+// slower on 64 vocabulary rows).  OSR_FORCE_KERNEL="lse:cs=<n>,st=<0|1>,
+// g=<n>" picks the cluster size, the staged or streaming form and the group
+// width (tests).
 struct LsePlan {
     int g = 1;
     int cs = 1;
@@ -376,7 +377,22 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     const int u = vec ? vec_elems(in_dt) : 1;
     const int64_t nunits = vec ? N / u : N;
     const int upt = 32 / u;  // the kernel's 32 elements per thread per tile
-    const int g = pow2ceil(cdiv(nunits, upt));
+    const char *force = getenv("OSR_FORCE_KERNEL");
+    const bool forced = force && strncmp(force, "lse", 3) == 0;
+    int g = pow2ceil(cdiv(nunits, upt));
+    if (g > 256) g = 256;
+    // 16-byte rows: narrower groups while each thread still streams at most
+    // 16 units (256 bytes: four bf16 tiles, two fp32 tiles) and the grid
+    // keeps at least 128 Ki threads.  Fewer threads a row mean fewer block
+    // reductions a row and, from 32 lanes down, several rows a CTA reduced
+    // by warp shuffles alone.  Measured at 65536 rows (fraction of the copy
+    // peak): bf16 4096 elements 0.80 -> 0.99 (g 128 -> 32), 2048 elements
+    // 0.58 -> 0.90 (64 -> 16), 1024 elements 0.59 -> 0.79 (32 -> 8); fp32
+    // 2048 elements 0.99 -> 1.06 (64 -> 32).
+    while (vec && g > 1 && cdiv(nunits, g / 2) <= 16 && M * (g / 2) >= 131072) g /= 2;
+    int64_t fg = 0;
+    if (forced && parse_kv(force, "g", &fg) && fg >= 1 && fg <= 256 && (fg & (fg - 1)) == 0)
+        g = (int)fg;  // a forced group width (tests)
     if (g <= 32) {
         lp.g = g;
         lp.grid = cdiv(M, 128 / g);
@@ -384,45 +400,48 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     }
     // one CTA per row: as many threads as one tile of the row needs, up to
     // 256 (a 4096-element bf16 row at 256 threads left half of them idle:
-    // 8192 such rows 36.2 -> 19.4 us at 128)
-    lp.g = g < 256 ? g : 256;
+    // 8192 such rows 36.2 -> 19.4 us at 128), or fewer as above
+    lp.g = g;
     int64_t cs = 1;
-    const char *force = getenv("OSR_FORCE_KERNEL");
     int64_t fcs = 0;
     const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
     // staged: 12 CTAs per row (16 for one or two rows), each piece
-    // bulk-copied whole, when the grid fits one wave (shared memory allows
-    // CTAs an SM by the piece).  Measured on 152064-element rows: staged was
-    // 11-26 % faster than streaming while it fit one wave (bf16 up to 96
-    // rows, fp32 up to 48: 32 bf16 rows 7.1 -> 5.3 us, 64 bf16 rows 8.6 ->
-    // 7.7 us) and up to 20 % slower beyond (64 fp32 rows: 10.4 -> 11.3 us).
+    // bulk-copied whole, for up to 32 rows whose pieces fit one wave.
+    // Measured on 152064-element rows against the streaming clusters below:
+    // 8 bf16 rows 3.6 us against 4.9, 32 rows 5.3 against 5.7; from 64 rows
+    // on the streaming clusters were faster (64 bf16 rows 7.4 against 7.9,
+    // 64 fp32 rows 9.2 against 11.8).
     bool staged_fit = false;
     int64_t cs_st = M <= 2 ? 16 : 12;
     if (cs_st > most) cs_st = most;
-    if (vec && cs_st > 1) {
+    if (vec && cs_st > 1 && M <= 32) {
         const int64_t smem = 128 + cdiv(nunits, cs_st) * 16;
         const int64_t per_sm = (int64_t)smem_per_sm / (smem + 1024);  // 1 KiB reserved a CTA
         const int64_t slots = (per_sm < 8 ? per_sm : 8) * sms;
         staged_fit = smem <= kStagedMaxSmem && M * cs_st <= slots;
     }
-    if (force && strncmp(force, "lse", 3) == 0 && parse_kv(force, "cs", &fcs) && fcs >= 1 && fcs <= 16) {
+    if (forced && parse_kv(force, "cs", &fcs) && fcs >= 1 && fcs <= 16) {
         cs = fcs;  // a forced cluster size (tests)
     } else if (staged_fit) {
         cs = cs_st;
-    } else if (M < 2 * (int64_t)sms) {
-        // streaming clusters, measured on 152064-element rows: 10 CTAs per
-        // row for up to 16 rows (18 % faster than 8), 4 for more (8 % faster
-        // than 8 at 64 rows)
-        cs = M <= 16 ? 10 : 4;
-        if (cs > most) cs = most;
-        if (cs < 1) cs = 1;
+    } else if (M <= 16) {
+        cs = 10;  // measured 18 % faster than 8 on up to 16 vocabulary rows
+    } else {
+        // streaming: about 512 CTAs in all, a power of two per row, at most
+        // 8.  Measured on 152064-element rows (bf16 / fp32, fraction of the
+        // copy peak): 96 rows at 4 0.48 / 0.73, 256 rows at 2 0.67 / 0.90
+        // against 0.60 / 0.84 at 4, 512 rows at 1 0.81 / 0.96.
+        cs = 1;
+        while (cs < 8 && M * cs * 2 <= 512) cs *= 2;
     }
+    if (cs > most) cs = most;
+    if (cs < 1) cs = 1;
     if (cs > 1) lp.g = 256;  // the cluster kernels run 256-thread CTAs
     lp.cs = (int)cs;
     lp.chunk = cdiv(nunits, cs);
     lp.grid = M * cs;
     int64_t st = staged_fit ? 1 : 0;
-    if (force && strncmp(force, "lse", 3) == 0) parse_kv(force, "st", &st);
+    if (forced) parse_kv(force, "st", &st);
     if (cs > 1 && vec && st != 0 && 128 + lp.chunk * 16 <= kStagedMaxSmem) {
         lp.staged = true;
         lp.smem = (size_t)(128 + lp.chunk * 16);

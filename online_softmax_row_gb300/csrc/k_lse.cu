@@ -7,11 +7,10 @@
 // each row once and writes two numbers per row: HBM traffic is the input
 // alone.
 //
-// Each thread streams its units in tiles.  A tile's maximum (and the first
-// index where it occurs) and its sum of exp(x - max) are folded into the
-// thread's running (m, d, index) with the (m, d) merge, the index following
-// the larger maximum (the earlier one on ties, since a thread visits its
-// elements in increasing order).  Across threads, CTAs and cluster CTAs:
+// Each thread streams its units in tiles and keeps a running (m, d): the
+// online normaliser's update, taken once per tile (the running maximum
+// raised by the tile's maximum, the sum rescaled, then the tile's exps
+// added against the new maximum).  Across threads, CTAs and cluster CTAs:
 // the row maximum, then the smallest index holding it, then the sum of
 // d e^(m_t - m).
 #include <cuda_runtime.h>
@@ -58,6 +57,84 @@ __device__ __forceinline__ MaxArgSum group_mas(MaxArgSum t) {
     return r;
 }
 
+// A thread's tile of the streaming kernel: NU units kept raw, 16-byte
+// vectors (U > 1) or single elements widened to binary32 (U = 1).
+template <bool B>
+struct LseFull {
+    static constexpr bool value = B;
+};
+template <int U>
+struct RawOf {
+    using T = uint4;
+};
+template <>
+struct RawOf<1> {
+    using T = float;
+};
+template <int U>
+using Raw = typename RawOf<U>::T;
+
+template <Dt DI, int U>
+__device__ __forceinline__ Raw<U> raw_neg_inf() {
+    if constexpr (U == 1) {
+        return -INFINITY;
+    } else {
+        const uint32_t n = DI == Dt::BF16 ? 0xff80ff80u : 0xff800000u;
+        return make_uint4(n, n, n, n);
+    }
+}
+// element k of a unit, exactly widened
+template <Dt DI, int U>
+__device__ __forceinline__ float raw_elem(const Raw<U> &q, int k) {
+    if constexpr (U == 1) {
+        return q;
+    } else if constexpr (DI == Dt::BF16) {
+        const uint32_t w = k < 2 ? q.x : k < 4 ? q.y : k < 6 ? q.z : q.w;
+        return (k & 1) ? bf16_hi(w) : bf16_lo(w);
+    } else {
+        return __uint_as_float(k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w);
+    }
+}
+// elements 2p and 2p + 1 of the tile as an f32x2 pair
+template <Dt DI, int U, int NU>
+__device__ __forceinline__ uint64_t raw_pair(const Raw<U> (&q)[NU], int p) {
+    if constexpr (U == 1)
+        return f2_make(q[2 * p], q[2 * p + 1]);
+    else
+        return f2_of<DI>(q[p / (U / 2)], p % (U / 2));
+}
+// the tile's maximum, as a tree (bfloat16 on packed pairs); a NaN loses
+// unless every element is NaN
+template <Dt DI, int U, int NU>
+__device__ __forceinline__ float raw_tile_max(const Raw<U> (&q)[NU]) {
+    if constexpr (U > 1 && DI == Dt::BF16) {
+        uint32_t w[NU];
+#pragma unroll
+        for (int j = 0; j < NU; ++j)
+            w[j] = lse_max_bf16x2(lse_max_bf16x2(q[j].x, q[j].y), lse_max_bf16x2(q[j].z, q[j].w));
+#pragma unroll
+        for (int h = NU / 2; h >= 1; h /= 2)
+#pragma unroll
+            for (int j = 0; j < h; ++j) w[j] = lse_max_bf16x2(w[j], w[j + h]);
+        return fmaxf(bf16_lo(w[0]), bf16_hi(w[0]));
+    } else {
+        float v[NU];
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            if constexpr (U == 1)
+                v[j] = q[j];
+            else
+                v[j] = fmaxf(fmaxf(__uint_as_float(q[j].x), __uint_as_float(q[j].y)),
+                             fmaxf(__uint_as_float(q[j].z), __uint_as_float(q[j].w)));
+        }
+#pragma unroll
+        for (int h = NU / 2; h >= 1; h /= 2)
+#pragma unroll
+            for (int j = 0; j < h; ++j) v[j] = fmaxf(v[j], v[j + h]);
+        return v[0];
+    }
+}
+
 template <Dt DI, int G, int U, bool CLUSTER>
 __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const RowArgs a) {
     constexpr int NU = kLseEpt / U;
@@ -81,122 +158,96 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
     }
     pdl_wait();
 
-    MaxArgSum t{-INFINITY, 0.f, kNoIndex};
-    if constexpr (U > 1) {
-        // 16-byte vectors kept raw: the tile's maximum on packed pairs
-        // (max.bf16x2; a NaN loses, as with fmaxf), its exps on f32x2 pairs,
-        // and the element index searched only when the running maximum
-        // grows (a thread visits its elements in increasing index order, so
-        // an equal maximum later never moves the first index)
-        if (s.ok) {
-            const uint64_t l2e = f2_make(1.4426950408889634f, 1.4426950408889634f);
-            const uint32_t neg_inf = DI == Dt::BF16 ? 0xff80ff80u : 0xff800000u;
-            for (int64_t base = s.u0; base < s.u1; base += (int64_t)G * NU) {
-                uint4 q[NU];
+    // The thread's running maximum m only grows: a tile that raises it
+    // rescales the running sum by e^(m_old - m_new) and records its base.
+    // The tile's exps are then taken against the running maximum (so no
+    // second exp per tile), summed on f32x2 pairs, and the tile's sum added
+    // whole to the running one.  The first index holding the maximum is
+    // searched once, after the group's maximum is known, and only by the
+    // threads that hold it: in the tile they recorded, which is still in
+    // registers when it was the last one (a thread visits its elements in
+    // increasing index order, so a later tile with the same maximum never
+    // moves the first index).  An in-loop search would run on whichever
+    // lanes raised their maximum in that tile, and the warp would pay for
+    // it on almost every tile.
+    float m_run = -INFINITY;
+    uint64_t d2 = f2_make(0.f, 0.f);
+    int64_t tbase = -1, last = -1;
+    Raw<U> q[NU];
+    auto load = [&](int64_t base, auto full) {
 #pragma unroll
-                for (int j = 0; j < NU; ++j) {
-                    const int64_t ui = base + (int64_t)j * G + s.t;
-                    q[j] = ui < s.u1 ? ld16<Hint::Stream>(xrow + ui * 16) : make_uint4(neg_inf, neg_inf, neg_inf, neg_inf);
-                }
-                float tm = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < NU; ++j) {
-                    if constexpr (DI == Dt::BF16) {
-                        const uint32_t w = lse_max_bf16x2(lse_max_bf16x2(q[j].x, q[j].y), lse_max_bf16x2(q[j].z, q[j].w));
-                        tm = fmaxf(tm, fmaxf(bf16_lo(w), bf16_hi(w)));
-                    } else {
-                        tm = fmaxf(fmaxf(tm, fmaxf(__uint_as_float(q[j].x), __uint_as_float(q[j].y))),
-                                   fmaxf(__uint_as_float(q[j].z), __uint_as_float(q[j].w)));
-                    }
-                }
-                const uint64_t tm2 = f2_make(md_shift(tm), md_shift(tm));
-                uint64_t acc = f2_make(0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < NU; ++j)
-#pragma unroll
-                    for (int k = 0; k < U / 2; ++k) {
-                        const uint64_t e = f2_mul(f2_sub(f2_of<DI>(q[j], k), tm2), l2e);
-                        acc = f2_add(acc, f2_make(ex2_approx(f2_lo(e)), ex2_approx(f2_hi(e))));
-                    }
-                const float td = f2_lo(acc) + f2_hi(acc);
-                if (tm > t.m) {
-                    int64_t ti = kNoIndex;
-#pragma unroll
-                    for (int j = NU - 1; j >= 0; --j)
-#pragma unroll
-                        for (int k = U - 1; k >= 0; --k) {
-                            float v;
-                            if constexpr (DI == Dt::BF16) {
-                                const uint32_t w = k < 2 ? q[j].x : k < 4 ? q[j].y : k < 6 ? q[j].z : q[j].w;
-                                v = (k & 1) ? bf16_hi(w) : bf16_lo(w);
-                            } else {
-                                v = __uint_as_float(k == 0 ? q[j].x : k == 1 ? q[j].y : k == 2 ? q[j].z : q[j].w);
-                            }
-                            if (v == tm) ti = (base + (int64_t)j * G + s.t) * U + k;  // the last hit is the first
-                        }
-                    t.d = t.d * expf(t.m - tm) + td;
-                    t.m = tm;
-                    t.i = ti;
+        for (int j = 0; j < NU; ++j) {
+            const int64_t ui = base + (int64_t)j * G + s.t;
+            if (decltype(full)::value || ui < s.u1) {
+                if constexpr (U > 1) {
+                    q[j] = ld16<Hint::Stream>(xrow + ui * 16);
                 } else {
-                    t.d += td * md_factor(tm, t.m);
+                    float v[1];
+                    load_unit<DI, 1>(xrow, ui, v);
+                    q[j] = v[0];
                 }
+            } else {
+                q[j] = raw_neg_inf<DI, U>();
             }
         }
-    } else {
-        if (s.ok) {
-            for (int64_t base = s.u0; base < s.u1; base += (int64_t)G * NU) {
-                float v[NU][U];
-#pragma unroll
-                for (int j = 0; j < NU; ++j) {
-                    const int64_t ui = base + (int64_t)j * G + s.t;
-                    if (ui < s.u1) {
-                        load_unit<DI, U>(xrow, ui * U, v[j]);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < U; ++k) v[j][k] = -INFINITY;
-                    }
-                }
-                float tm = -INFINITY;
-                int64_t ti = kNoIndex;
-#pragma unroll
-                for (int j = 0; j < NU; ++j)
-#pragma unroll
-                    for (int k = 0; k < U; ++k)
-                        if (v[j][k] > tm) {
-                            tm = v[j][k];
-                            ti = (base + (int64_t)j * G + s.t) * U + k;
-                        }
-                float td = 0.f;
-#pragma unroll
-                for (int j = 0; j < NU; ++j)
-#pragma unroll
-                    for (int k = 0; k < U; ++k) td += exp_shifted(v[j][k], md_shift(tm));
-                if (tm > t.m) {
-                    t.d = t.d * expf(t.m - tm) + td;
-                    t.m = tm;
-                    t.i = ti;
-                } else {
-                    t.d += td * md_factor(tm, t.m);
-                    if (tm == t.m && ti < t.i) t.i = ti;
-                }
+    };
+    if (s.ok && s.u1 > s.u0) {
+        const int64_t step = (int64_t)G * NU;
+        last = s.u0 + (s.u1 - s.u0 - 1) / step * step;
+        const uint64_t l2e = f2_make(1.4426950408889634f, 1.4426950408889634f);
+        auto run = [&](int64_t base, auto full) {
+            load(base, full);
+            const float tm = raw_tile_max<DI, U, NU>(q);
+            if (tm > m_run) {  // false for -inf and for an all-NaN tile
+                const float f = md_factor(m_run, tm);
+                d2 = f2_mul(d2, f2_make(f, f));
+                m_run = tm;
+                tbase = base;
             }
-        }
+            const float ms = md_shift(m_run);
+            const uint64_t m2 = f2_make(ms, ms);
+            uint64_t acc = f2_make(0.f, 0.f);
+#pragma unroll
+            for (int p = 0; p < NU * U / 2; ++p) {
+                const uint64_t e = f2_mul(f2_sub(raw_pair<DI, U>(q, p), m2), l2e);
+                acc = f2_add(acc, f2_make(ex2_approx(f2_lo(e)), ex2_approx(f2_hi(e))));
+            }
+            d2 = f2_add(d2, acc);
+        };
+        for (int64_t base = s.u0; base < last; base += step) run(base, LseFull<true>{});
+        run(last, LseFull<false>{});
     }
+    const float dsum = f2_lo(d2) + f2_hi(d2);
+    // first index of m in the recorded tile (reloaded unless it was the last)
+    auto first_index = [&]() -> int64_t {
+        if (tbase != last) load(tbase, LseFull<true>{});
+        int64_t ti = kNoIndex;
+#pragma unroll
+        for (int j = NU - 1; j >= 0; --j)
+#pragma unroll
+            for (int k = U - 1; k >= 0; --k)
+                if (raw_elem<DI, U>(q[j], k) == m_run) ti = (tbase + (int64_t)j * G + s.t) * U + k;
+        return ti;  // the last hit is the first
+    };
 
     MaxArgSum r;
     if constexpr (G <= 32) {
-        r = group_mas<G>(t);
+        r.m = group_max<G>(m_run);
+        const int64_t ti = tbase >= 0 && m_run == r.m ? first_index() : kNoIndex;
+        r.i = group_min_i64<G>(ti);
+        r.d = group_sum<G>(dsum * md_factor(m_run, r.m));
     } else {
         constexpr int NW = RowsGeom<G>::kWarps;
         __shared__ float s_m[32], s_d[32];
         __shared__ long long s_i[32];
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        float m = group_max<32>(t.m);
+        float m = group_max<32>(m_run);
         if (lane == 0) s_m[warp] = m;
         __syncthreads();
         m = group_max<NW>(s_m[lane & (NW - 1)]);
-        const int64_t wi = group_min_i64<32>(t.m == m ? t.i : kNoIndex);
-        const float wd = group_sum<32>(t.d * md_factor(t.m, m));
+        const int64_t ti = tbase >= 0 && m_run == m ? first_index() : kNoIndex;
+        const int64_t wi = group_min_i64<32>(ti);
+        const float wd = group_sum<32>(dsum * md_factor(m_run, m));
         if (lane == 0) {
             s_d[warp] = wd;
             s_i[warp] = wi;

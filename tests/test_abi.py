@@ -229,13 +229,19 @@ def test_forced_kernel(monkeypatch):
 
 
 def test_logsumexp_plans_and_validation(lib):
-    # staged while 12 CTAs a row fit one wave (bf16 pieces 25 KiB: 8 an SM;
-    # fp32 pieces 50 KiB: 4 an SM), streaming clusters of 4 beyond
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 96, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
+    # staged for up to 32 rows while 12 CTAs a row fit one wave (bf16 pieces
+    # 25 KiB: 8 an SM; fp32 pieces 50 KiB: 4 an SM); beyond, streaming
+    # clusters of a power of two CTAs, about 512 CTAs in all, at most 8
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 33, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 96, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 128, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "f32") == "lse-cluster g=256 cs=4 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 152064, "bf16") == "lse-cluster g=256 cs=2 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 512, 152064, "bf16") == "lse-rows g=256 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 32768, "bf16") == "lse-cluster g=256 cs=4 vec"  # a full tile each
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 1, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32", vec_ok=False) == "lse-cluster g=256 cs=10 scalar"
@@ -278,8 +284,12 @@ def test_topk_plans_and_validation(lib, monkeypatch):
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=8 piece=38016B vec"
     monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16,st=0")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=16 vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16,st=1")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")  # the staged form where the planner stages
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
+    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:g=32")
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 4096, 4096, "bf16") == "lse-rows g=32 cs=1 vec"
     monkeypatch.delenv("OSR_FORCE_KERNEL")
     T = lib.osr_row_topk
     assert T(P, P * 8, P * 16, None, None, 0, 16, 4, F32, None) == 0            # M == 0

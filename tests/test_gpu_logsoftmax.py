@@ -142,11 +142,49 @@ def test_row_logsumexp_ties_and_edges():
         assert am.cpu().tolist() == [7, 7, 7]
 
 
-def test_vocab_workload_sampling_statistics():
-    w = workloads.WORKLOADS["logsumexp_argmax_vocab_bf16_64x152064"]
+@pytest.mark.parametrize("name", [n for n, w in workloads.WORKLOADS.items() if w.op == "logsumexp"])
+def test_logsumexp_workloads_full_size(name):
+    # every row of every log-sum-exp workload, in the launch the benchmark
+    # times, checked a block of rows at a time
+    w = workloads.WORKLOADS[name]
     x = workloads.make(w)["x"]
     lse, am = osr.row_logsumexp(x.cuda())
     torch.cuda.synchronize()
+    lse, am = lse.cpu(), am.cpu()
+    step = max(1, (1 << 24) // w.N)
+    for r0 in range(0, w.M, step):
+        check_lse(x[r0:r0 + step], lse[r0:r0 + step], am[r0:r0 + step])
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("dt,misaligned", [("bf16", False), ("f32", False), ("bf16", True)])
+def test_logsumexp_forced_group_widths(g, dt, misaligned):
+    # a thread streams many tiles; rows whose maximum sits in the first tile
+    # (so its first index is searched in a reloaded tile), in the last one,
+    # tied across tiles, and a ragged tail
+    M, N = 37, 5003 if misaligned else 5000
+    x = case(M, N, dt, seed_of("lse-g", g, dt, misaligned)).float()
+    top = 4000.0  # above every sample, shifted rows (+1000) included
+    x[0, 3] = top
+    x[1, N - 1] = top
+    x[2, 5] = top
+    x[2, N - 7] = top
+    x[3, 1] = top
+    x[3, 2] = top
+    x = x.to(DT[dt])
+    xd = x.cuda()
+    if misaligned:
+        buf = torch.empty(M * N + 1, dtype=x.dtype, device="cuda")
+        xd = buf[1:].view(M, N)
+        xd.copy_(x.cuda())
+    os.environ["OSR_FORCE_KERNEL"] = f"lse:g={g}"
+    try:
+        assert osr.plan_describe(osr.OP_LOGSUMEXP, M, N, dt, vec_ok=not misaligned).startswith(f"lse-rows g={g} ")
+        lse, am = osr.row_logsumexp(xd)
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["OSR_FORCE_KERNEL"]
+    assert am.cpu().tolist()[:4] == [3, N - 1, 5, 1]
     check_lse(x, lse, am)
 
 

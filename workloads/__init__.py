@@ -97,6 +97,14 @@ WORKLOADS["logsumexp_argmax_vocab_bf16_64x152064"] = Workload(
     "logsumexp_argmax_vocab_bf16_64x152064", "logsumexp", 64, 152064, "bf16", "f32", sigma=4.0,
     spikes_per_row=8, l2_resident=True,
     note="sampling statistics of the vocabulary-logit rows: log-sum-exp and argmax, no probabilities")
+WORKLOADS["logsumexp_argmax_vocab_bf16_1024x152064"] = Workload(
+    "logsumexp_argmax_vocab_bf16_1024x152064", "logsumexp", 1024, 152064, "bf16", "f32", sigma=4.0,
+    spikes_per_row=8,
+    note="sampling statistics of a 1024-row batch of vocabulary-logit rows (311 MB)")
+WORKLOADS["logsumexp_attn_bf16_114688x4096"] = Workload(
+    "logsumexp_attn_bf16_114688x4096", "logsumexp", 28 * 4096, 4096, "bf16", "f32", sigma=3.0,
+    shift_rows=round(0.01 * 28 * 4096),
+    note="per-query log-sum-exp of bf16 attention scores, 28 heads x 4096 x 4096, 1% rows +1000")
 WORKLOADS["topk_vocab_bf16_64x152064_k50"] = Workload(
     "topk_vocab_bf16_64x152064_k50", "topk", 64, 152064, "bf16", "f32", sigma=4.0,
     spikes_per_row=8, l2_resident=True, k=50,
