@@ -390,9 +390,24 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     // 0.58 -> 0.90 (64 -> 16), 1024 elements 0.59 -> 0.79 (32 -> 8); fp32
     // 2048 elements 0.99 -> 1.06 (64 -> 32).
     while (vec && g > 1 && cdiv(nunits, g / 2) <= 16 && M * (g / 2) >= 131072) g /= 2;
+    // long 16-byte rows, 128 rows or more: one CTA of up to 1024 threads per
+    // row instead of a cluster, as wide as keeps about 16 MB of tiles in
+    // flight over the grid while each thread still streams two tiles or
+    // more.  Measured on 152064-element rows (fraction of the copy peak,
+    // against the clusters / 256-thread CTAs the planner chose before):
+    // bf16 128 rows 0.58 against 0.56 (1024 threads), 256 rows 0.75 against
+    // 0.67 (1024), 512 rows 0.85 against 0.81 (512); fp32 128 rows 0.84
+    // against 0.80, 256 rows 0.94 against 0.92; bf16 32768-element rows at
+    // 256 rows 0.44 against 0.39 (512).
+    int gw = g;
+    if (vec && g == 256 && M >= 128) {
+        const int64_t tile = 16 * (int64_t)upt;  // bytes a thread loads per tile
+        while (gw < 1024 && M * (gw * 2) * tile <= ((int64_t)1 << 24) && nunits >= (int64_t)gw * 4 * upt)
+            gw *= 2;
+    }
     int64_t fg = 0;
-    if (forced && parse_kv(force, "g", &fg) && fg >= 1 && fg <= 256 && (fg & (fg - 1)) == 0)
-        g = (int)fg;  // a forced group width (tests)
+    if (forced && parse_kv(force, "g", &fg) && fg >= 1 && fg <= 1024 && (fg & (fg - 1)) == 0)
+        g = gw = (int)fg;  // a forced group width (tests)
     if (g <= 32) {
         lp.g = g;
         lp.grid = cdiv(M, 128 / g);
@@ -400,7 +415,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     }
     // one CTA per row: as many threads as one tile of the row needs, up to
     // 256 (a 4096-element bf16 row at 256 threads left half of them idle:
-    // 8192 such rows 36.2 -> 19.4 us at 128), or fewer as above
+    // 8192 such rows 36.2 -> 19.4 us at 128), or fewer or more as above
     lp.g = g;
     int64_t cs = 1;
     int64_t fcs = 0;
@@ -426,17 +441,20 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
         cs = cs_st;
     } else if (M <= 16) {
         cs = 10;  // measured 18 % faster than 8 on up to 16 vocabulary rows
+    } else if (gw > 256) {
+        cs = 1;  // the wide CTAs above
     } else {
         // streaming: about 512 CTAs in all, a power of two per row, at most
-        // 8.  Measured on 152064-element rows (bf16 / fp32, fraction of the
-        // copy peak): 96 rows at 4 0.48 / 0.73, 256 rows at 2 0.67 / 0.90
-        // against 0.60 / 0.84 at 4, 512 rows at 1 0.81 / 0.96.
+        // 8.  Measured (bf16 / fp32, fraction of the copy peak): 152064-
+        // element rows, 64 rows at 8 0.39 / 0.62, 96 rows at 4 0.48 / 0.73;
+        // 32768-element bf16 rows, 128 rows at 4 0.25 against 0.23 at 1.
         cs = 1;
         while (cs < 8 && M * cs * 2 <= 512) cs *= 2;
     }
     if (cs > most) cs = most;
     if (cs < 1) cs = 1;
     if (cs > 1) lp.g = 256;  // the cluster kernels run 256-thread CTAs
+    else if (gw > 256) lp.g = gw;
     lp.cs = (int)cs;
     lp.chunk = cdiv(nunits, cs);
     lp.grid = M * cs;

@@ -460,7 +460,7 @@ cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cu
 #define OSR_MAKE(G) \
     if (g == G) fn = lse_argmax_kernel<DI, G, U, false>;
     OSR_MAKE(1) OSR_MAKE(2) OSR_MAKE(4) OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(64)
-    OSR_MAKE(128) OSR_MAKE(256)
+    OSR_MAKE(128) OSR_MAKE(256) OSR_MAKE(512) OSR_MAKE(1024)
 #undef OSR_MAKE
     if (!fn) return cudaErrorInvalidConfiguration;
     return launch_fn(fn, grid, g <= 32 ? RowsGeom<1>::kThreads : g, 0, a, st);

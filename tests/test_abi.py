@@ -236,9 +236,15 @@ def test_logsumexp_plans_and_validation(lib):
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 33, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 96, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 128, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 152064, "bf16") == "lse-cluster g=256 cs=2 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 512, 152064, "bf16") == "lse-rows g=256 cs=1 vec"
+    # from 128 rows: one CTA of up to 1024 threads per row (about 16 MB of
+    # tiles in flight over the grid, two tiles a thread at least)
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 128, 152064, "bf16") == "lse-rows g=1024 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 152064, "bf16") == "lse-rows g=1024 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 512, 152064, "bf16") == "lse-rows g=512 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 1024, 152064, "bf16") == "lse-rows g=256 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 152064, "f32") == "lse-rows g=512 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 32768, "bf16") == "lse-rows g=512 cs=1 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 16384, "bf16") == "lse-cluster g=256 cs=2 vec"  # too short to widen
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 32768, "bf16") == "lse-cluster g=256 cs=4 vec"  # a full tile each

@@ -156,7 +156,7 @@ def test_logsumexp_workloads_full_size(name):
         check_lse(x[r0:r0 + step], lse[r0:r0 + step], am[r0:r0 + step])
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024])
 @pytest.mark.parametrize("dt,misaligned", [("bf16", False), ("f32", False), ("bf16", True)])
 def test_logsumexp_forced_group_widths(g, dt, misaligned):
     # a thread streams many tiles; rows whose maximum sits in the first tile
