@@ -598,7 +598,7 @@ struct TopkPlan {
 constexpr size_t kTopkSmemLimit = 227 * 1024 - 256;  // dynamic shared memory per CTA
 
 osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, int sms,
-                     int max_cluster, TopkPlan *tp) {
+                     int max_cluster, int smem_per_sm, TopkPlan *tp) {
     *tp = TopkPlan();
     const int eb = elem_bytes(dt);
     const int u = vec ? vec_elems(dt) : 1;
@@ -610,13 +610,43 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
         if (!parse_kv(force, "cs", &fcs) || fcs < 1) return OSR_ERR_UNSUPPORTED;
         cs = fcs;
         tp->forced = true;
+    } else if (M > 96) {
+        // many rows: each CTA's time is mostly a chain of short phases, so
+        // what counts is how many rows an SM works on at once -- the CTAs an
+        // SM holds by shared memory (at most 4, the register bound) over the
+        // CTAs a row needs; on a tie, the fewest CTAs a row that still puts
+        // two on an SM (a lone CTA an SM leaves its copy and phases
+        // unoverlapped: 262144 bf16 elements at 3 CTAs a row, one an SM,
+        // 0.28 against 0.33 at 6, two an SM).  Measured at 512-2048
+        // rows (fraction of the copy peak, against the 6 CTAs a row before):
+        // bf16 152064 elements 3 CTAs 0.34 against 0.31, 65536 elements 3
+        // 0.33 against 0.20, 32768 elements 2 0.24 against 0.11; fp32 32768
+        // elements 3 0.35 against 0.21; fp32 152064 and bf16 262144 stay at 6.
+        int64_t best = 0, best_per = 0;
+        for (int64_t c = cs_min; c <= kTopkMaxCluster && c <= max_cluster; ++c) {
+            if (c > cs_min && cdiv(N, c) < (int64_t)kTopkThreads * u) break;  // under a vector a thread
+            const int64_t ch = cdiv(cdiv(N, c), u) * u;
+            if (ch * eb > kTopkMaxPieceBytes) continue;
+            int64_t r = ch * eb > pow2_at_least(k) * 8 ? ch * eb : pow2_at_least(k) * 8;
+            if (r < kTopkMinWords * 8) r = kTopkMinWords * 8;
+            const int64_t sm = (int64_t)topk_smem_bytes((uint32_t)cdiv(r, 16) * 16, k);
+            if (sm > kTopkSmemLimit) continue;
+            int64_t per = smem_per_sm / (sm + kTopkStaticSmem + 1024);  // 1 KiB reserved a CTA
+            if (per > 4) per = 4;
+            if (per == 0) continue;
+            if (best == 0 || per * best > best_per * c || (per * best == best_per * c && best_per < 2 && per > best_per)) {
+                best = c;
+                best_per = per;
+            }
+        }
+        if (best > 0) cs = best;
     } else {
-        // measured on 1-256 rows of 152064 elements: 8 CTAs per row for up to
+        // measured on 1-96 rows of 152064 elements: 8 CTAs per row for up to
         // 16 rows (3-5 % faster than 12 with the row-wide bound, 7-11 %
-        // faster than 16), 4 up to 96 rows (10 % faster than 8 at 64), 6
-        // beyond; never fewer than the row needs, and never so many that a
-        // CTA gets less than one vector per thread
-        const int64_t fill = M <= 16 ? 8 : M <= 96 ? 4 : 6;
+        // faster than 16), 4 up to 96 rows (10 % faster than 8 at 64); never
+        // fewer than the row needs, and never so many that a CTA gets less
+        // than one vector per thread
+        const int64_t fill = M <= 16 ? 8 : 4;
         if (fill > cs) cs = fill;
         while (cs > cs_min && cdiv(N, cs) < (int64_t)kTopkThreads * u) cs = cs / 2 > cs_min ? cs / 2 : cs_min;
     }
@@ -770,7 +800,7 @@ osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_
     if (op == 6) {  // top-k: the plan for k = 64 (k changes only the sort buffer)
         const bool tvec = vec_ok && (N % vec_elems(in_dt)) == 0;
         TopkPlan tp;
-        const osr_status ts = topk_plan(M, N, N < 64 ? N : 64, in_dt, tvec, sm_count, 16, &tp);
+        const osr_status ts = topk_plan(M, N, N < 64 ? N : 64, in_dt, tvec, sm_count, 16, kSmemPerSmDefault, &tp);
         if (ts != OSR_OK) return ts;
         snprintf(buf, buf_len, "topk cs=%d piece=%lldB %s", tp.cs,
                  (long long)(tp.chunk * elem_bytes(in_dt)), tvec ? "vec" : "scalar");
@@ -1001,7 +1031,7 @@ osr_status osr_row_topk(const void *x, float *values, int64_t *indices, float *p
     if ((s = device_info(&di)) != OSR_OK) return s;
     const bool vec = aligned16(x) && N % vec_elems(in_dt) == 0;
     TopkPlan tp;
-    if ((s = topk_plan(M, N, k, in_dt, vec, di.sms, di.max_cluster, &tp)) != OSR_OK) return s;
+    if ((s = topk_plan(M, N, k, in_dt, vec, di.sms, di.max_cluster, di.smem_per_sm, &tp)) != OSR_OK) return s;
     if (M * tp.cs > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
     // the cluster shape must be schedulable with this much shared memory
     int n = 0;

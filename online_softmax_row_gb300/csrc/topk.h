@@ -33,6 +33,9 @@ constexpr int kTopkMaxCluster = 16;
 constexpr int kTopkListCap = 1024;  // keys at or above a CTA's bound kept in a short list
 constexpr int64_t kTopkRankMaxK = 256;  // k up to this: outputs placed by counting, no sort
 constexpr int64_t kTopkMinWords = 2048;  // the piece region holds at least this many 8-byte words
+// the kernel's static shared memory (1552 bytes as built), for the planner's
+// estimate of CTAs per SM
+constexpr int64_t kTopkStaticSmem = 1600;
 
 // Dynamic shared memory of one CTA: piece (or sort buffer), the histogram,
 // the published histogram (two buffers), the short list, the candidates.

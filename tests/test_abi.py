@@ -279,7 +279,12 @@ def test_topk_plans_and_validation(lib, monkeypatch):
     D = osr.plan_describe
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
     assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=8 piece=38016B vec"    # few rows: 8 CTAs
-    assert D(osr.OP_TOPK, 256, 152064, "bf16") == "topk cs=6 piece=50688B vec"
+    # many rows: the cluster size that keeps the most rows in flight per SM
+    assert D(osr.OP_TOPK, 256, 152064, "bf16") == "topk cs=3 piece=101376B vec"
+    assert D(osr.OP_TOPK, 256, 152064, "f32") == "topk cs=6 piece=101376B vec"
+    assert D(osr.OP_TOPK, 2048, 32768, "bf16") == "topk cs=1 piece=65536B vec"
+    assert D(osr.OP_TOPK, 2048, 65536, "bf16") == "topk cs=3 piece=43696B vec"
+    assert D(osr.OP_TOPK, 2048, 262144, "bf16") == "topk cs=6 piece=87392B vec"
     assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=4 piece=152064B vec"
     assert D(osr.OP_TOPK, 8, 1000, "bf16") == "topk cs=1 piece=2000B vec"       # short rows: one CTA
     assert D(osr.OP_TOPK, 3, 33, "bf16", vec_ok=False) == "topk cs=1 piece=66B scalar"

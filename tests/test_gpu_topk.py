@@ -79,6 +79,17 @@ def test_topk(M, N, k, dt):
     check(x, k, *out, what=f"{M}x{N} k={k} {dt}")
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,k", [(130, 152064, 50), (200, 32768, 50), (120, 65536, 64), (98, 5000, 8)])
+def test_topk_many_rows(M, N, k, dt):
+    # more than 96 rows: the planner's rows-in-flight cluster sizes (1, 3 or
+    # 6 CTAs a row here), every row checked
+    x = rows(M, N, dt, seed=M * 7 + N + k)
+    out = osr.row_topk(x.cuda(), k)
+    torch.cuda.synchronize()
+    check(x, k, *out, what=f"{M}x{N} k={k} {dt}")
+
+
 @pytest.mark.parametrize("cs", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_topk_forced_cluster_sizes(cs, dt):
