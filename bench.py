@@ -610,7 +610,8 @@ def ours(args):
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
     peak, peak_src = measured_peaks()
     w = workloads.WORKLOADS[args.workload]
-    if args.max_rows and w.M > args.max_rows:
+    capped = bool(args.max_rows and w.M > args.max_rows)
+    if capped:
         # profiling a smaller case of the same kernel (same row length, plan
         # and per-row work): traffic then scales by rows
         w = dataclasses.replace(w, M=args.max_rows,
@@ -654,14 +655,15 @@ def ours(args):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "in_dtype": w.in_dtype,
                    "out_dtype": w.out_dtype, "min_bytes_per_step": w.min_bytes, "kernel": plan,
-                   "rows_capped": bool(args.max_rows and w.M == args.max_rows),
+                   "rows_capped": capped,
                    "timing": ("the steps issued one by one on the stream" if args.stream_launches else
                               "CUDA graph of the steps (programmatic dependent launch edges), captured "
                               "before the timed region; CUDA events around one replay"),
                    "l2": f"rotating {n_sets_for(w, l2)} input/output sets (> 2x L2 of traffic "
                          f"between reuses); no flush", "parallelism": f"rows; {world} GPU(s), weak"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w, plan),
+                     # the committed captures are of the full-size workloads
+                     "frac": round(achieved / peak, 4), "traffic": None if capped else profiled_traffic(w, plan),
                      "kernel_source_hash": source_hash(w),
                      "peak_source": peak_src + " -- of measured" if "measured" in peak_src else peak_src,
                      "algorithmic_bytes_per_launch": w.min_bytes // launches_per_call(plan, w.M)},
