@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const
             load(base, full);
             const float tm = raw_tile_max<DI, U, NU>(q);
             if (tm > m_run) {  // false for -inf and for an all-NaN tile
-                const float f = md_factor(m_run, tm);
+                // e^(m_run - tm) by the terms' own exp: 0 from m_run = -inf
+                // (and for tm = +inf), no guard needed
+                const float f = exp_shifted(m_run, tm);
                 d2 = f2_mul(d2, f2_make(f, f));
                 m_run = tm;
                 tbase = base;
