@@ -421,15 +421,16 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     int64_t fcs = 0;
     const int64_t most = cdiv(nunits, 256 * (int64_t)upt);  // at least a full tile each
     // staged: 12 CTAs per row (16 for one or two rows), each piece
-    // bulk-copied whole, for up to 32 rows whose pieces fit one wave.
-    // Measured on 152064-element rows against the streaming clusters below:
-    // 8 bf16 rows 3.6 us against 4.9, 32 rows 5.3 against 5.7; from 64 rows
-    // on the streaming clusters were faster (64 bf16 rows 7.4 against 7.9,
-    // 64 fp32 rows 9.2 against 11.8).
+    // bulk-copied whole, for up to 8 rows long enough for 12 CTAs of full
+    // tiles, whose pieces fit one wave.  Measured against 10 streaming CTAs
+    // a row: 152064-element rows, 1 bf16 row 3.0 us against 3.4, 8 rows 3.6
+    // against 3.8 (fp32 4.0 against 4.0), 12 rows 4.0 against 3.9 (fp32 4.7
+    // against 4.3); 32768-element rows (4 CTAs of full tiles) 3.0 against
+    // 2.7 at every row count from 1 to 24.
     bool staged_fit = false;
     int64_t cs_st = M <= 2 ? 16 : 12;
     if (cs_st > most) cs_st = most;
-    if (vec && cs_st > 1 && M <= 32) {
+    if (vec && M <= 8 && most >= 12) {
         const int64_t smem = 128 + cdiv(nunits, cs_st) * 16;
         const int64_t per_sm = (int64_t)smem_per_sm / (smem + 1024);  // 1 KiB reserved a CTA
         const int64_t slots = (per_sm < 8 ? per_sm : 8) * sms;
@@ -439,14 +440,19 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
         cs = fcs;  // a forced cluster size (tests)
     } else if (staged_fit) {
         cs = cs_st;
-    } else if (M <= 16) {
-        cs = 10;  // measured 18 % faster than 8 on up to 16 vocabulary rows
+    } else if (M * 10 <= 512) {
+        // 10 streaming CTAs a row while that keeps the grid near 512 CTAs.
+        // Measured on 152064-element rows (us, against 8 / 12 a row): bf16
+        // 24 rows 4.5 against 5.2 / 4.9, 32 rows 5.1 against 5.4 / 5.2, 48
+        // rows 6.0 against 6.3 / 6.5; fp32 32 rows 6.1 against 6.4 / 6.2
+        cs = 10;
     } else if (gw > 256) {
         cs = 1;  // the wide CTAs above
     } else {
         // streaming: about 512 CTAs in all, a power of two per row, at most
         // 8.  Measured (bf16 / fp32, fraction of the copy peak): 152064-
-        // element rows, 64 rows at 8 0.39 / 0.62, 96 rows at 4 0.48 / 0.73;
+        // element rows, 64 rows at 8 0.39 / 0.62 (10 a row: fp32 16 %
+        // slower, the grid past one wave), 96 rows at 4 0.48 / 0.73;
         // 32768-element bf16 rows, 128 rows at 4 0.25 against 0.23 at 1.
         cs = 1;
         while (cs < 8 && M * cs * 2 <= 512) cs *= 2;

@@ -229,13 +229,18 @@ def test_forced_kernel(monkeypatch):
 
 
 def test_logsumexp_plans_and_validation(lib):
-    # staged for up to 32 rows while 12 CTAs a row fit one wave (bf16 pieces
-    # 25 KiB: 8 an SM; fp32 pieces 50 KiB: 4 an SM); beyond, streaming
-    # clusters of a power of two CTAs, about 512 CTAs in all, at most 8
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 33, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
+    # staged for up to 8 rows long enough for 12 CTAs of full tiles (bf16
+    # pieces 25 KiB: 8 an SM; fp32 pieces 50 KiB: 4 an SM); 10 streaming
+    # CTAs a row up to 51 rows, then a power of two, about 512 CTAs in all
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 9, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 51, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 52, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 96, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 4, 32768, "bf16") == "lse-cluster g=256 cs=4 vec"  # too short to stage
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "f32") == "lse-cluster g=256 cs=10 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 32768, "bf16") == "lse-cluster g=256 cs=4 vec"  # a full tile each
     # from 128 rows: one CTA of up to 1024 threads per row (about 16 MB of
     # tiles in flight over the grid, two tiles a thread at least)
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 128, 152064, "bf16") == "lse-rows g=1024 cs=1 vec"
@@ -245,9 +250,8 @@ def test_logsumexp_plans_and_validation(lib):
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 152064, "f32") == "lse-rows g=512 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 32768, "bf16") == "lse-rows g=512 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 16384, "bf16") == "lse-cluster g=256 cs=2 vec"  # too short to widen
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 32768, "bf16") == "lse-cluster g=256 cs=4 vec"  # a full tile each
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-cluster g=256 cs=10 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 1, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32", vec_ok=False) == "lse-cluster g=256 cs=10 scalar"
@@ -298,7 +302,7 @@ def test_topk_plans_and_validation(lib, monkeypatch):
     monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16,st=1")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")  # the staged form where the planner stages
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:g=32")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 4096, 4096, "bf16") == "lse-rows g=32 cs=1 vec"
     monkeypatch.delenv("OSR_FORCE_KERNEL")

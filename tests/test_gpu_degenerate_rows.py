@@ -143,7 +143,7 @@ def test_in_place_softmax_degenerate_rows(spec, dt):
 # log-sum-exp / argmax: short rows (groups of lanes), one CTA per row, the
 # streaming cluster, the staged cluster, and narrow groups whose threads
 # stream many tiles
-LSE_TIERS = [(None, 64), (None, 5000), ("lse:cs=4,st=0", 152064), ("lse:cs=12", 152064),
+LSE_TIERS = [(None, 64), (None, 5000), ("lse:cs=4,st=0", 152064), ("lse:cs=12,st=1", 152064),
              ("lse:cs=3,st=1", 40000), ("lse:cs=2,st=0", 5001),
              ("lse:g=1", 5000), ("lse:g=8", 4096),  # many tiles a thread
              ("lse:g=1024,cs=1", 40000)]            # one wide CTA a row

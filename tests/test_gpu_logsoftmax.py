@@ -200,7 +200,7 @@ def test_log_softmax_vocab_workload_full_size():
 def test_row_logsumexp_staged_edges(dt):
     # few rows: pieces staged in shared memory; a -inf row, a NaN, ties split
     # over CTAs, and a row whose maximum sits in the last piece
-    N = 65536
+    N = 131072
     x = torch.randn(4, N, generator=torch.Generator().manual_seed(17)) * 3
     x[0] = -float("inf")
     x[1, 40000] = float("nan")
