@@ -156,6 +156,18 @@ def test_logsumexp_workloads_full_size(name):
         check_lse(x[r0:r0 + step], lse[r0:r0 + step], am[r0:r0 + step])
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("M", [8, 9, 51, 52, 127, 128, 512])
+def test_logsumexp_plan_boundaries(M, dt):
+    # the row counts where the planner changes tier on vocabulary rows:
+    # staged -> 10 streaming CTAs -> a power of two -> wide CTAs
+    N = 152064
+    x = case(M, N, dt, seed_of("lse-bound", M, dt), sigma=4.0)
+    lse, am = osr.row_logsumexp(x.cuda())
+    torch.cuda.synchronize()
+    check_lse(x, lse, am)
+
+
 @pytest.mark.parametrize("g", [1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024])
 @pytest.mark.parametrize("dt,misaligned", [("bf16", False), ("f32", False), ("bf16", True)])
 def test_logsumexp_forced_group_widths(g, dt, misaligned):

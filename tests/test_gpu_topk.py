@@ -80,7 +80,8 @@ def test_topk(M, N, k, dt):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("M,N,k", [(130, 152064, 50), (200, 32768, 50), (120, 65536, 64), (98, 5000, 8)])
+@pytest.mark.parametrize("M,N,k", [(96, 152064, 50), (97, 152064, 50), (130, 152064, 50), (200, 32768, 50),
+                                   (120, 65536, 64), (98, 5000, 8)])
 def test_topk_many_rows(M, N, k, dt):
     # more than 96 rows: the planner's rows-in-flight cluster sizes (1, 3 or
     # 6 CTAs a row here), every row checked
