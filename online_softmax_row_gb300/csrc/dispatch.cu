@@ -440,11 +440,15 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
         cs = fcs;  // a forced cluster size (tests)
     } else if (staged_fit) {
         cs = cs_st;
-    } else if (M * 10 <= 512) {
-        // 10 streaming CTAs a row while that keeps the grid near 512 CTAs.
-        // Measured on 152064-element rows (us, against 8 / 12 a row): bf16
-        // 24 rows 4.5 against 5.2 / 4.9, 32 rows 5.1 against 5.4 / 5.2, 48
-        // rows 6.0 against 6.3 / 6.5; fp32 32 rows 6.1 against 6.4 / 6.2
+    } else if (M * 10 * 10 <= (int64_t)9 * sms * lse_cluster_ctas_per_sm(in_dt == OSR_BF16 ? Dt::BF16 : Dt::F32)) {
+        // 10 streaming CTAs a row while the grid fits one wave: the CTAs the
+        // kernel holds an SM (5 bf16, 4 fp32) times the SMs, less a tenth
+        // for clusters that do not pack into a GPC.  Measured on 152064-
+        // element rows (us, against 8 / 12 a row): bf16 24 rows 4.5 against
+        // 5.2 / 4.9, 48 rows 5.8 against 6.2 / 6.4, 64 rows 6.8 against
+        // 7.1 / 8.8 (80 rows: 9.1 against 8.0 at 8, past one wave); fp32
+        // 32 rows 6.1 against 6.4 / 6.2, 56 rows 8.0 against 8.5 (64 rows:
+        // 10.7 against 9.2 at 8)
         cs = 10;
     } else if (gw > 256) {
         cs = 1;  // the wide CTAs above

@@ -136,7 +136,8 @@ __device__ __forceinline__ float raw_tile_max(const Raw<U> (&q)[NU]) {
 }
 
 template <Dt DI, int G, int U, bool CLUSTER>
-__global__ void __launch_bounds__(RowsGeom<G>::kThreads) lse_argmax_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads, CLUSTER ? lse_cluster_ctas_per_sm(DI) : 0)
+lse_argmax_kernel(const RowArgs a) {
     constexpr int NU = kLseEpt / U;
     const int64_t nunits = a.N / U;
     const Slice s = make_slice<G, CLUSTER>(a, nunits);

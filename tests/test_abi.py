@@ -231,12 +231,13 @@ def test_forced_kernel(monkeypatch):
 def test_logsumexp_plans_and_validation(lib):
     # staged for up to 8 rows long enough for 12 CTAs of full tiles (bf16
     # pieces 25 KiB: 8 an SM; fp32 pieces 50 KiB: 4 an SM); 10 streaming
-    # CTAs a row up to 51 rows, then a power of two, about 512 CTAs in all
+    # CTAs a row while the grid fits one wave (bf16 up to 68 rows, fp32 up
+    # to 54), then a power of two, about 512 CTAs in all
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "bf16") == "lse-staged g=256 cs=12 piece=25344B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 9, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 51, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 52, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 68, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 69, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=10 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 96, 152064, "bf16") == "lse-cluster g=256 cs=4 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 4, 32768, "bf16") == "lse-cluster g=256 cs=4 vec"  # too short to stage
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 32, 152064, "f32") == "lse-cluster g=256 cs=10 vec"
@@ -250,8 +251,8 @@ def test_logsumexp_plans_and_validation(lib):
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 152064, "f32") == "lse-rows g=512 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 32768, "bf16") == "lse-rows g=512 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 256, 16384, "bf16") == "lse-cluster g=256 cs=2 vec"  # too short to widen
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 48, 152064, "f32") == "lse-cluster g=256 cs=10 vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 54, 152064, "f32") == "lse-cluster g=256 cs=10 vec"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 55, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 1, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32", vec_ok=False) == "lse-cluster g=256 cs=10 scalar"

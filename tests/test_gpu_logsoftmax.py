@@ -157,10 +157,11 @@ def test_logsumexp_workloads_full_size(name):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-@pytest.mark.parametrize("M", [8, 9, 51, 52, 127, 128, 512])
+@pytest.mark.parametrize("M", [8, 9, 54, 55, 68, 69, 127, 128, 512])
 def test_logsumexp_plan_boundaries(M, dt):
     # the row counts where the planner changes tier on vocabulary rows:
-    # staged -> 10 streaming CTAs -> a power of two -> wide CTAs
+    # staged -> 10 streaming CTAs (to 68 bf16 / 54 fp32 rows) -> a power of
+    # two -> wide CTAs
     N = 152064
     x = case(M, N, dt, seed_of("lse-bound", M, dt), sigma=4.0)
     lse, am = osr.row_logsumexp(x.cuda())
