@@ -22,6 +22,7 @@
 #include "../../include/osr.h"
 #include "../../include/osr_test.h"
 #include "launch.h"
+#include "lse.h"
 #include "staged.h"
 #include "topk.h"
 

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "lse.h"
 
 namespace osr {
 

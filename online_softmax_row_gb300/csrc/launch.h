@@ -94,9 +94,6 @@ cudaError_t rmsnorm_cluster_occupancy(int g, bool vec, int cs, int *n);
 template <Dt DI>
 cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t grid,
                        cudaStream_t st);
-// CTAs an SM the streaming cluster kernel is compiled to hold (its launch
-// bound: registers are capped to fit), which the planner counts on
-constexpr int lse_cluster_ctas_per_sm(Dt d) { return d == Dt::BF16 ? 5 : 4; }
 // Staged variant (16-byte rows): a.cs CTAs per row, each bulk-copying its
 // piece of a.chunk units into `smem` bytes of shared memory (128 + piece).
 template <Dt DI>
