@@ -229,8 +229,8 @@ int osr_last_cuda_error(void);
  *             the compute entry points read the current device's figure
  *   buf       receives a NUL-terminated description, e.g.
  *             "rows g=256 ept=16 vec" or "cluster cs=10 g=1024 ept=16 vec"
- * Honours the OSR_FORCE_KERNEL environment variable exactly as the
- * compute entry points do.  Returns OSR_ERR_INVALID on bad arguments.
+ * Honours a plan forced with osr_test_force_kernel (osr_test.h) exactly as
+ * the compute entry points do.  Returns OSR_ERR_INVALID on bad arguments.
  */
 osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out_dt,
                              int vec_ok, int sm_count, char *buf, size_t buf_len);

@@ -1,7 +1,7 @@
 /*
  * osr_test.h -- test support of the GB300 row-wise reduce-then-rescale
- * library.  These entry points exist so that tests can reach two internals
- * the computation itself never exposes; no computation path calls them, and
+ * library.  These entry points exist so that tests can reach internals the
+ * computation itself never exposes; no computation path calls them, and
  * the operations they serve have no counterpart on the pages the library
  * follows.
  */
@@ -25,6 +25,18 @@ extern "C" {
  */
 #define OSR_TEST_NO_ARRIVE 1
 int osr_test_set_flags(int flags);
+
+/*
+ * Force the dispatcher's choice for every later call of the calling process
+ * (compute entry points and osr_plan_describe alike) until cleared with
+ * NULL or "".  The spec names a tier and its shape, e.g. "rows:g=512",
+ * "cluster:g=256,cs=2", "staged:cs=3,r=8", "split:s=7,b=3", "lse:cs=4,st=0",
+ * "lse:g=32", "topk:cs=8"; a shape the tier cannot take makes the calls
+ * return OSR_ERR_UNSUPPORTED.  The spec is copied (at most 63 characters,
+ * else OSR_ERR_INVALID).  Tests use it to run every tier on chosen shapes;
+ * with none set the planners read nothing but an atomic flag.
+ */
+osr_status osr_test_force_kernel(const char *spec);
 
 /*
  * The kernels' e^(x - m), evaluated on the device beside CUDA's expf, so a

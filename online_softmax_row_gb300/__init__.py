@@ -21,9 +21,11 @@ plan_describe        osr_plan_describe
 bench_copy           osr_bench_copy
 bench_memcpy         osr_bench_memcpy
 device_fault         osr_device_fault
+forced_kernel        osr_test_force_kernel (test support, osr_test.h)
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -35,7 +37,8 @@ from . import build as _build
 __all__ = ["OsrError", "rmsnorm_fwd", "layernorm_fwd", "OP_LAYERNORM", "fused_add_rmsnorm", "softmax_rows", "softmax_rows_stats",
            "log_softmax_rows", "row_logsumexp", "row_topk", "OP_LOG_SOFTMAX", "OP_LOGSUMEXP",
            "OP_TOPK",
-           "plan_describe", "bench_copy", "bench_memcpy", "device_fault", "library", "library_path", "OP_RMSNORM",
+           "plan_describe", "bench_copy", "bench_memcpy", "device_fault", "forced_kernel", "library",
+           "library_path", "OP_RMSNORM",
            "OP_FUSED",
            "OP_SOFTMAX"]
 
@@ -88,10 +91,11 @@ def library():
         lib.osr_layernorm_fwd.argtypes = [P, P, P, F, P, I64, I64, I, P]
         lib.osr_row_logsumexp.argtypes = [P, P, P, I64, I64, I, P]
         lib.osr_row_topk.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
+        lib.osr_test_force_kernel.argtypes = [ctypes.c_char_p]
         for fn in ("osr_rmsnorm_fwd", "osr_fused_add_rmsnorm", "osr_softmax_rows",
                    "osr_softmax_rows_stats", "osr_plan_describe", "osr_bench_copy", "osr_bench_memcpy",
                    "osr_device_fault", "osr_log_softmax_rows", "osr_row_logsumexp", "osr_row_topk",
-                   "osr_layernorm_fwd"):
+                   "osr_layernorm_fwd", "osr_test_force_kernel"):
             getattr(lib, fn).restype = I
         _lib = lib
         return lib
@@ -313,3 +317,17 @@ def device_fault(device=None) -> int:
     if st not in (0, 6):
         _check(st, "osr_device_fault")
     return v.value
+
+
+@contextlib.contextmanager
+def forced_kernel(spec: str | None):
+    """Test support: every call inside the block (and plan_describe) uses the
+    forced plan `spec` (e.g. "rows:g=512", "staged:cs=3,r=8", "lse:g=32",
+    "topk:cs=8"; see include/osr_test.h); None or "" forces nothing.  The
+    previous state, none, is restored on exit."""
+    lib = library()
+    _check(lib.osr_test_force_kernel(spec.encode() if spec else None), "osr_test_force_kernel")
+    try:
+        yield
+    finally:
+        lib.osr_test_force_kernel(None)

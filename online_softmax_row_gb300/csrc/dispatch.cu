@@ -34,6 +34,26 @@ thread_local int g_last_cuda_error = 0;
 // osr_test_set_flags (include/osr_test.h): read once per staged launch
 std::atomic<int> g_test_flags{0};
 
+// osr_test_force_kernel (include/osr_test.h): a forced plan for tests,
+// copied under a lock; the planners read it only while one is set
+std::atomic<bool> g_force_set{false};
+std::mutex g_force_mu;
+char g_force[64] = "";
+
+struct ForceSpec {
+    char s[64];
+    const char *get() const { return s[0] ? s : nullptr; }
+};
+ForceSpec forced_spec() {
+    ForceSpec f;
+    f.s[0] = 0;
+    if (g_force_set.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_force_mu);
+        memcpy(f.s, g_force, sizeof f.s);
+    }
+    return f;
+}
+
 osr_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
     return OSR_ERR_CUDA;
@@ -242,7 +262,8 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
     const int64_t nunits = vec ? N / p->u : N;
     const int in_bytes = elem_bytes(in_dt);
 
-    const char *force = getenv("OSR_FORCE_KERNEL");
+    const ForceSpec force_spec = forced_spec();
+    const char *force = force_spec.get();
     if (force && *force) {
         p->forced = true;
         int64_t g = 0, cs = 0, s = 0, b = 0;
@@ -361,7 +382,7 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
 // only has to spread the rows.  Short rows: a group of g <= 32 lanes per row.
 // Otherwise one CTA per row, or a cluster of CTAs per row while there are
 // too few rows to fill the GPU (sizes below; 16-CTA clusters were 70 %
-// slower on 64 vocabulary rows).  OSR_FORCE_KERNEL="lse:cs=<n>,st=<0|1>,
+// slower on 64 vocabulary rows).  A forced spec "lse:cs=<n>,st=<0|1>,
 // g=<n>" picks the cluster size, the staged or streaming form and the group
 // width (tests).
 struct LsePlan {
@@ -378,7 +399,8 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     const int u = vec ? vec_elems(in_dt) : 1;
     const int64_t nunits = vec ? N / u : N;
     const int upt = 32 / u;  // the kernel's 32 elements per thread per tile
-    const char *force = getenv("OSR_FORCE_KERNEL");
+    const ForceSpec force_spec = forced_spec();
+    const char *force = force_spec.get();
     const bool forced = force && strncmp(force, "lse", 3) == 0;
     int g = pow2ceil(cdiv(nunits, upt));
     if (g > 256) g = 256;
@@ -596,7 +618,7 @@ osr_status check_cluster_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_
 // the row (at most kTopkMaxPieceBytes) in shared memory.  The fewest CTAs
 // that hold the row, raised by the row count (below), but never so far that
 // a CTA gets less than one vector per thread.
-// OSR_FORCE_KERNEL="topk:cs=<n>" picks cs (tests).
+// A forced spec "topk:cs=<n>" (osr_test_force_kernel) picks cs (tests).
 struct TopkPlan {
     int cs = 1;
     int64_t chunk = 0;
@@ -615,7 +637,8 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
     const int u = vec ? vec_elems(dt) : 1;
     const int64_t cs_min = cdiv(N * eb, kTopkMaxPieceBytes);
     int64_t cs = cs_min;
-    const char *force = getenv("OSR_FORCE_KERNEL");
+    const ForceSpec force_spec = forced_spec();
+    const char *force = force_spec.get();
     int64_t fcs = 0;
     if (force && strncmp(force, "topk", 4) == 0) {
         if (!parse_kv(force, "cs", &fcs) || fcs < 1) return OSR_ERR_UNSUPPORTED;
@@ -799,6 +822,18 @@ const char *osr_status_string(osr_status s) {
 int osr_last_cuda_error(void) { return g_last_cuda_error; }
 
 int osr_test_set_flags(int flags) { return g_test_flags.exchange(flags); }
+
+osr_status osr_test_force_kernel(const char *spec) {
+    if (spec && strlen(spec) >= sizeof g_force) return OSR_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_force_mu);
+    if (spec) {
+        strcpy(g_force, spec);
+    } else {
+        g_force[0] = 0;
+    }
+    g_force_set.store(g_force[0] != 0, std::memory_order_release);
+    return OSR_OK;
+}
 
 int osr_version(void) { return 100; }
 

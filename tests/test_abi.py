@@ -195,35 +195,55 @@ def test_split_shape_bounds():
     assert 1 <= s <= 512 and 1 <= b <= 3
 
 
-def test_forced_kernel(monkeypatch):
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "split:s=7,b=3")
+@pytest.fixture
+def force(lib):
+    """Set a forced plan (osr_test_force_kernel); cleared after the test."""
+    def set_spec(spec):
+        assert lib.osr_test_force_kernel(spec.encode() if spec else None) == 0
+    yield set_spec
+    lib.osr_test_force_kernel(None)
+
+
+def test_force_kernel_setter(lib, force):
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("rows g=")
+    force("split:s=7,b=3")
     assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("split s=7 b=3")
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "cluster:g=256,cs=2")
+    force("")  # an empty spec forces nothing
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("rows g=")
+    assert lib.osr_test_force_kernel(b"x" * 64) == 1  # longer than 63 characters
+    force(None)
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("rows g=")
+
+
+def test_forced_kernel(force):
+    force("split:s=7,b=3")
+    assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("split s=7 b=3")
+    force("cluster:g=256,cs=2")
     assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("cluster cs=2 g=256")
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "rows:g=512")
+    force("rows:g=512")
     assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("rows g=512")
     # a forced shape that cannot hold the row is refused, not silently changed
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "rows:g=64")
+    force("rows:g=64")
     with pytest.raises(osr.OsrError) as e:
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
     assert e.value.name == "OSR_ERR_UNSUPPORTED"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "cluster:g=256,cs=1")
+    force("cluster:g=256,cs=1")
     with pytest.raises(osr.OsrError):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3")
+    force("staged:cs=3")
     assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32").startswith("staged cs=3 g=256 piece=6672B")
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3,r=8")
+    force("staged:cs=3,r=8")
     assert osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32") == "staged cs=3 g=256 piece=6672B r=8 vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3,g=128,r=8")  # only the compiled shapes
+    force("staged:cs=3,g=128,r=8")  # only the compiled shapes
     with pytest.raises(osr.OsrError):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=3,r=5")
+    force("staged:cs=3,r=5")
     with pytest.raises(osr.OsrError):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
     for bad in ((osr.OP_RMSNORM, True), (osr.OP_SOFTMAX, False)):  # softmax, 16-byte rows only
         with pytest.raises(osr.OsrError):
             osr.plan_describe(bad[0], 10, 5000, "f32", vec_ok=bad[1])
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "staged:cs=17")
+    force("staged:cs=17")
     with pytest.raises(osr.OsrError):
         osr.plan_describe(osr.OP_SOFTMAX, 10, 5000, "f32")
 
@@ -280,7 +300,7 @@ def test_layernorm_plans_and_validation(lib):
     assert lib.osr_layernorm_fwd(None, None, None, f, None, 0, 16, F32, None) == 0
 
 
-def test_topk_plans_and_validation(lib, monkeypatch):
+def test_topk_plans_and_validation(lib, force):
     D = osr.plan_describe
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
     assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=8 piece=38016B vec"    # few rows: 8 CTAs
@@ -296,17 +316,17 @@ def test_topk_plans_and_validation(lib, monkeypatch):
     assert D(osr.OP_TOPK, 1, 786432, "f32") == "topk cs=16 piece=196608B vec"   # largest row
     with pytest.raises(osr.OsrError):
         D(osr.OP_TOPK, 1, 786433, "f32")                                        # beyond 16 x 192 KiB
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "topk:cs=8")
+    force("topk:cs=8")
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=8 piece=38016B vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16,st=0")
+    force("lse:cs=16,st=0")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-cluster g=256 cs=16 vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16,st=1")
+    force("lse:cs=16,st=1")
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:cs=16")  # the staged form where the planner stages
+    force("lse:cs=16")  # the staged form where the planner stages
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
-    monkeypatch.setenv("OSR_FORCE_KERNEL", "lse:g=32")
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 4096, 4096, "bf16") == "lse-rows g=32 cs=1 vec"
-    monkeypatch.delenv("OSR_FORCE_KERNEL")
+    force("lse:g=32")
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 64, 4096, "bf16") == "lse-rows g=32 cs=1 vec"
+    force(None)
     T = lib.osr_row_topk
     assert T(P, P * 8, P * 16, None, None, 0, 16, 4, F32, None) == 0            # M == 0
     assert T(P, P * 8, P * 16, None, None, 4, 16, 0, F32, None) == 1            # k < 1

@@ -68,19 +68,10 @@ def degenerate_rows(N: int, dt: str, seed: int) -> torch.Tensor:
 
 
 def run_forced(spec, fn):
-    old = os.environ.get("OSR_FORCE_KERNEL")
-    if spec:
-        os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         out = fn()
         torch.cuda.synchronize()
         return out
-    finally:
-        if spec:
-            if old is None:
-                del os.environ["OSR_FORCE_KERNEL"]
-            else:
-                os.environ["OSR_FORCE_KERNEL"] = old
 
 
 def all_minus_inf(xo: np.ndarray) -> np.ndarray:

@@ -41,14 +41,13 @@ def test_wait_timeout_is_reported_and_context_survives(spec):
     x = workloads.softmax_inputs(1, 32768, "f32", sigma=2.0, seed=1)["x"].cuda()
     poison = torch.full((1, 32768), 0x7FC0DEAD, dtype=torch.int32, device="cuda")
     y = poison.view(torch.float32)
-    os.environ["OSR_FORCE_KERNEL"] = spec
     assert set_test_flags(NO_ARRIVE) == 0
     try:
-        assert osr.plan_describe(osr.OP_SOFTMAX, 1, 32768, "f32").startswith("staged cs=2")
-        osr.softmax_rows(x, out=y)
+        with osr.forced_kernel(spec):
+            assert osr.plan_describe(osr.OP_SOFTMAX, 1, 32768, "f32").startswith("staged cs=2")
+            osr.softmax_rows(x, out=y)
     finally:
         assert set_test_flags(0) == NO_ARRIVE
-        del os.environ["OSR_FORCE_KERNEL"]
     assert osr.device_fault() == 1          # the bounded wait ran out and said so
     assert torch.all(poison == 0x7FC0DEAD)  # no stores after the failed wait
     assert osr.device_fault() == 0          # reading clears the word

@@ -98,12 +98,9 @@ def test_layernorm_mean_101_stress(dt):
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_layernorm_every_tier(spec, dt):
     x, g, b = ln_case(37, 5000, dt, seed_of("lnt", spec, dt), 100.0, 102.0)
-    os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         y = osr.layernorm_fwd(x.cuda(), g.cuda(), b.cuda(), EPS)
         torch.cuda.synchronize()
-    finally:
-        del os.environ["OSR_FORCE_KERNEL"]
     check_ln(x, g, b, y)
 
 
@@ -113,24 +110,16 @@ def test_layernorm_in_place_and_misaligned(spec):
     buf = torch.empty(6 * 4001 + 1, device="cuda")
     xm = buf[1:].view(6, 4001)
     xm.copy_(x.cuda())
-    if spec:
-        os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         osr.layernorm_fwd(xm, g.cuda(), b.cuda(), EPS, out=xm)
         torch.cuda.synchronize()
-    finally:
-        os.environ.pop("OSR_FORCE_KERNEL", None)
     check_ln(x, g, b, xm)
     # aligned, in place, through every tier
     x2, g2, b2 = ln_case(5, 8192, "bf16", seed_of("lnip2", spec))
     xc = x2.cuda()
-    if spec:
-        os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         osr.layernorm_fwd(xc, g2.cuda(), b2.cuda(), EPS, out=xc)
         torch.cuda.synchronize()
-    finally:
-        os.environ.pop("OSR_FORCE_KERNEL", None)
     check_ln(x2, g2, b2, xc)
 
 

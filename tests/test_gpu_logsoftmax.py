@@ -73,12 +73,9 @@ def test_log_softmax(M, N, io):
 @pytest.mark.parametrize("spec", ["rows:g=512", "cluster:g=256,cs=5", "staged:cs=3", "split:s=6,b=4"])
 def test_log_softmax_every_tier(spec):
     x = case(37, 5000, "f32", seed_of("logtier", spec))
-    os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         y = osr.log_softmax_rows(x.cuda())
         torch.cuda.synchronize()
-    finally:
-        del os.environ["OSR_FORCE_KERNEL"]
     check_log(x, y)
 
 
@@ -190,13 +187,10 @@ def test_logsumexp_forced_group_widths(g, dt, misaligned):
         buf = torch.empty(M * N + 1, dtype=x.dtype, device="cuda")
         xd = buf[1:].view(M, N)
         xd.copy_(x.cuda())
-    os.environ["OSR_FORCE_KERNEL"] = f"lse:g={g}"
-    try:
+    with osr.forced_kernel(f"lse:g={g}"):
         assert osr.plan_describe(osr.OP_LOGSUMEXP, M, N, dt, vec_ok=not misaligned).startswith(f"lse-rows g={g} ")
         lse, am = osr.row_logsumexp(xd)
         torch.cuda.synchronize()
-    finally:
-        del os.environ["OSR_FORCE_KERNEL"]
     assert am.cpu().tolist()[:4] == [3, N - 1, 5, 1]
     check_lse(x, lse, am)
 
@@ -234,10 +228,7 @@ def test_row_logsumexp_staged_edges(dt):
                                   "lse:cs=4,st=0", "lse:cs=10,st=0"])
 def test_logsumexp_forced_cluster_sizes(spec):
     x = case(6, 152064, "bf16", seed_of("lse-cs", spec))
-    os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         lse, am = osr.row_logsumexp(x.cuda())
         torch.cuda.synchronize()
-    finally:
-        del os.environ["OSR_FORCE_KERNEL"]
     check_lse(x, lse, am)

@@ -36,17 +36,10 @@ def gpu():
 
 
 def run_forced(spec, fn):
-    old = os.environ.get("OSR_FORCE_KERNEL")
-    os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         out = fn()
         torch.cuda.synchronize()
         return out
-    finally:
-        if old is None:
-            del os.environ["OSR_FORCE_KERNEL"]
-        else:
-            os.environ["OSR_FORCE_KERNEL"] = old
 
 
 # ------------------------------------------------------------ RMSNorm

@@ -55,17 +55,10 @@ def check(x_cpu, k, values, indices, probs, lse, what=""):
 
 
 def run_forced(spec, fn):
-    old = os.environ.get("OSR_FORCE_KERNEL")
-    os.environ["OSR_FORCE_KERNEL"] = spec
-    try:
+    with osr.forced_kernel(spec):
         out = fn()
         torch.cuda.synchronize()
         return out
-    finally:
-        if old is None:
-            del os.environ["OSR_FORCE_KERNEL"]
-        else:
-            os.environ["OSR_FORCE_KERNEL"] = old
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
