@@ -385,7 +385,12 @@ osr_status make_plan(Op op, int64_t M, int64_t N, osr_dtype in_dt, osr_dtype out
 // slower on 64 vocabulary rows).  A forced spec "lse:cs=<n>,st=<0|1>,
 // g=<n>" picks the cluster size, the staged or streaming form and the group
 // width (tests).
+// rows of at least this many elements that are not 16-byte aligned (or not a
+// whole number of vectors) stream their aligned bodies in vectors
+constexpr int64_t kLsePeelMinN = 64;
+
 struct LsePlan {
+    bool peel = false;  // rows not 16-byte aligned: vector bodies, element edges
     int g = 1;
     int cs = 1;
     int64_t chunk = 0;
@@ -394,14 +399,21 @@ struct LsePlan {
     size_t smem = 0;      // staged: dynamic shared memory per CTA
 };
 
-LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int smem_per_sm) {
+LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, bool peel, int sms,
+                 int smem_per_sm) {
     LsePlan lp;
-    const int u = vec ? vec_elems(in_dt) : 1;
-    const int64_t nunits = vec ? N / u : N;
-    const int upt = 32 / u;  // the kernel's 32 elements per thread per tile
     const ForceSpec force_spec = forced_spec();
     const char *force = force_spec.get();
     const bool forced = force && strncmp(force, "lse", 3) == 0;
+    int64_t fg0 = 0;
+    // a peeled row needs a lane per edge element: a forced narrower group
+    // takes the element path
+    if (peel && forced && parse_kv(force, "g", &fg0) && fg0 < vec_elems(in_dt)) peel = false;
+    lp.peel = peel && !vec;
+    vec = vec || lp.peel;  // the geometry of 16-byte units from here on
+    const int u = vec ? vec_elems(in_dt) : 1;
+    const int64_t nunits = vec ? N / u : N;
+    const int upt = 32 / u;  // the kernel's 32 elements per thread per tile
     int g = pow2ceil(cdiv(nunits, upt));
     if (g > 256) g = 256;
     // 16-byte rows: narrower groups while each thread still streams at most
@@ -431,6 +443,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     int64_t fg = 0;
     if (forced && parse_kv(force, "g", &fg) && fg >= 1 && fg <= 1024 && (fg & (fg - 1)) == 0)
         g = gw = (int)fg;  // a forced group width (tests)
+    if (lp.peel && g < u) g = u;
     if (g <= 32) {
         lp.g = g;
         lp.grid = cdiv(M, 128 / g);
@@ -453,7 +466,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     bool staged_fit = false;
     int64_t cs_st = M <= 2 ? 16 : 12;
     if (cs_st > most) cs_st = most;
-    if (vec && M <= 8 && most >= 12) {
+    if (vec && !lp.peel && M <= 8 && most >= 12) {
         const int64_t smem = 128 + cdiv(nunits, cs_st) * 16;
         const int64_t per_sm = (int64_t)smem_per_sm / (smem + 1024);  // 1 KiB reserved a CTA
         const int64_t slots = (per_sm < 8 ? per_sm : 8) * sms;
@@ -493,7 +506,7 @@ LsePlan lse_plan(int64_t M, int64_t N, osr_dtype in_dt, bool vec, int sms, int s
     lp.grid = M * cs;
     int64_t st = staged_fit ? 1 : 0;
     if (forced) parse_kv(force, "st", &st);
-    if (cs > 1 && vec && st != 0 && 128 + lp.chunk * 16 <= kStagedMaxSmem) {
+    if (cs > 1 && vec && !lp.peel && st != 0 && 128 + lp.chunk * 16 <= kStagedMaxSmem) {
         lp.staged = true;
         lp.smem = (size_t)(128 + lp.chunk * 16);
     }
@@ -856,13 +869,15 @@ osr_status osr_plan_describe(int op, int64_t M, int64_t N, osr_dtype in_dt, osr_
     if (s != OSR_OK) return s;
     const bool vec = vec_ok && (N % vec_elems(in_dt)) == 0;
     if (op == 4) {
-        const LsePlan lp = lse_plan(M, N, in_dt, vec, sm_count, kSmemPerSmDefault);
+        const LsePlan lp = lse_plan(M, N, in_dt, vec, !vec && N >= kLsePeelMinN, sm_count,
+                                    kSmemPerSmDefault);
+        const char *path = lp.peel ? "peel" : vec ? "vec" : "scalar";
         if (lp.staged)
             snprintf(buf, buf_len, "lse-staged g=%d cs=%d piece=%lldB %s", lp.g, lp.cs,
-                     (long long)lp.chunk * 16, vec ? "vec" : "scalar");
+                     (long long)lp.chunk * 16, path);
         else
             snprintf(buf, buf_len, "%s g=%d cs=%d %s", lp.cs > 1 ? "lse-cluster" : "lse-rows", lp.g,
-                     lp.cs, vec ? "vec" : "scalar");
+                     lp.cs, path);
         return OSR_OK;
     }
     Plan p;
@@ -1035,7 +1050,8 @@ osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t
     DeviceInfo di;
     if ((s = device_info(&di)) != OSR_OK) return s;
     const bool vec = aligned16(x) && N % vec_elems(in_dt) == 0;
-    const LsePlan lp = lse_plan(M, N, in_dt, vec, di.sms, di.smem_per_sm);
+    const bool peel = !vec && N >= kLsePeelMinN && (uintptr_t)x % elem_bytes(in_dt) == 0;
+    const LsePlan lp = lse_plan(M, N, in_dt, vec, peel, di.sms, di.smem_per_sm);
     if (lp.grid > 0x7fffffffLL) return OSR_ERR_UNSUPPORTED;
     RowArgs a = {};
     a.x = x;
@@ -1048,6 +1064,8 @@ osr_status osr_row_logsumexp(const void *x, float *lse, int64_t *argmax, int64_t
     const cudaError_t e =
         lp.staged ? (in_dt == OSR_F32 ? launch_lse_staged<Dt::F32>(a, lp.grid, lp.smem, (cudaStream_t)stream)
                                       : launch_lse_staged<Dt::BF16>(a, lp.grid, lp.smem, (cudaStream_t)stream))
+        : lp.peel ? (in_dt == OSR_F32 ? launch_lse_peel<Dt::F32>(a, lp.g, lp.cs > 1, lp.grid, (cudaStream_t)stream)
+                                      : launch_lse_peel<Dt::BF16>(a, lp.g, lp.cs > 1, lp.grid, (cudaStream_t)stream))
         : in_dt == OSR_F32 ? launch_lse<Dt::F32>(a, lp.g, lp.cs > 1, vec, lp.grid, (cudaStream_t)stream)
                            : launch_lse<Dt::BF16>(a, lp.g, lp.cs > 1, vec, lp.grid, (cudaStream_t)stream);
     return e == cudaSuccess ? OSR_OK : cuda_fail(e);

@@ -136,13 +136,36 @@ __device__ __forceinline__ float raw_tile_max(const Raw<U> (&q)[NU]) {
     }
 }
 
-template <Dt DI, int G, int U, bool CLUSTER>
-__global__ void __launch_bounds__(RowsGeom<G>::kThreads, CLUSTER ? lse_cluster_ctas_per_sm(DI) : 0)
+// PEEL: rows that do not start on a 16-byte boundary, or whose length is not
+// a multiple of the vector width.  Each row's body, from its first 16-byte
+// boundary, streams in 16-byte vectors as above; its head (the h < U
+// elements before that boundary) and its tail (the < U elements after the
+// last whole vector) are folded in one element a lane, the head before the
+// body and the tail after it (CTA 0 of a cluster).  Groups are at least U
+// lanes wide.  The bf16 256-thread form is held to 32 registers (eight CTAs
+// an SM, as the aligned one): 1024 rows of 50257 elements 22.7 -> 19.4 us,
+// the time of 50256-element aligned rows.
+template <Dt DI, int G, int U, bool CLUSTER, bool PEEL = false>
+__global__ void __launch_bounds__(RowsGeom<G>::kThreads,
+                                  CLUSTER ? lse_cluster_ctas_per_sm(DI)
+                                          : (PEEL && DI == Dt::BF16 && G == 256) ? 8 : 0)
 lse_argmax_kernel(const RowArgs a) {
     constexpr int NU = kLseEpt / U;
+    static_assert(!PEEL || (U > 1 && G >= U), "a peeled row needs vectors and a lane per edge element");
     const int64_t nunits = a.N / U;
-    const Slice s = make_slice<G, CLUSTER>(a, nunits);
-    const char *xrow = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+    Slice s = make_slice<G, CLUSTER>(a, nunits);
+    const char *row0 = reinterpret_cast<const char *>(a.x) + s.row * a.N * Elem<DI>::kBytes;
+    const char *xrow = row0;
+    int64_t h = 0, nb = nunits;  // head elements, body vectors
+    int tl = 0;                  // tail elements
+    if constexpr (PEEL) {
+        h = (int64_t)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(row0) & 15u)) & 15u) / Elem<DI>::kBytes);
+        if (h > a.N) h = a.N;
+        nb = (a.N - h) / U;
+        tl = (int)(a.N - h - nb * U);
+        if (s.u1 > nb) s.u1 = nb;
+        xrow = row0 + h * Elem<DI>::kBytes;  // 16-byte aligned
+    }
     // cluster: each CTA stores its (m, d, index) into slot [its rank] of
     // every CTA (st.async, counted on the receiver's xbar); no cluster
     // barrier after this start-up one
@@ -175,7 +198,25 @@ lse_argmax_kernel(const RowArgs a) {
     float m_run = -INFINITY;
     uint64_t d2 = f2_make(0.f, 0.f);
     int64_t tbase = -1, last = -1;
+    int64_t xidx = kNoIndex;  // PEEL: the edge element that set the running maximum
     Raw<U> q[NU];
+    // PEEL: element e of the row folded in like a one-element tile
+    auto fold_edge = [&](int64_t e) {
+        float v[1];
+        load_unit<DI, 1>(row0, e, v);
+        if (v[0] > m_run) {
+            const float f = exp_shifted(m_run, v[0]);
+            d2 = f2_mul(d2, f2_make(f, f));
+            m_run = v[0];
+            tbase = -1;
+            xidx = e;
+        }
+        d2 = f2_add(d2, f2_make(exp_shifted(v[0], md_shift(m_run)), 0.f));
+    };
+    const bool edges = PEEL && s.ok && s.u0 == 0;  // this CTA folds the row's edges
+    if constexpr (PEEL) {
+        if (edges && s.t < h) fold_edge(s.t);
+    }
     auto load = [&](int64_t base, auto full) {
 #pragma unroll
         for (int j = 0; j < NU; ++j) {
@@ -207,6 +248,7 @@ lse_argmax_kernel(const RowArgs a) {
                 d2 = f2_mul(d2, f2_make(f, f));
                 m_run = tm;
                 tbase = base;
+                if constexpr (PEEL) xidx = kNoIndex;
             }
             const float ms = md_shift(m_run);
             const uint64_t m2 = f2_make(ms, ms);
@@ -221,23 +263,29 @@ lse_argmax_kernel(const RowArgs a) {
         for (int64_t base = s.u0; base < last; base += step) run(base, LseFull<true>{});
         run(last, LseFull<false>{});
     }
+    if constexpr (PEEL) {
+        if (edges && s.t < tl) fold_edge(h + nb * U + s.t);
+    }
     const float dsum = f2_lo(d2) + f2_hi(d2);
     // first index of m in the recorded tile (reloaded unless it was the last)
+    // (PEEL: or the edge element that set it, which comes first)
     auto first_index = [&]() -> int64_t {
+        if (PEEL && xidx != kNoIndex) return xidx;
         if (tbase != last) load(tbase, LseFull<true>{});
         int64_t ti = kNoIndex;
 #pragma unroll
         for (int j = NU - 1; j >= 0; --j)
 #pragma unroll
             for (int k = U - 1; k >= 0; --k)
-                if (raw_elem<DI, U>(q[j], k) == m_run) ti = (tbase + (int64_t)j * G + s.t) * U + k;
+                if (raw_elem<DI, U>(q[j], k) == m_run) ti = h + (tbase + (int64_t)j * G + s.t) * U + k;
         return ti;  // the last hit is the first
     };
+    const bool holds = tbase >= 0 || (PEEL && xidx != kNoIndex);  // a recorded place of m_run
 
     MaxArgSum r;
     if constexpr (G <= 32) {
         r.m = group_max<G>(m_run);
-        const int64_t ti = tbase >= 0 && m_run == r.m ? first_index() : kNoIndex;
+        const int64_t ti = holds && m_run == r.m ? first_index() : kNoIndex;
         r.i = group_min_i64<G>(ti);
         r.d = group_sum<G>(dsum * md_factor(m_run, r.m));
     } else {
@@ -249,7 +297,7 @@ lse_argmax_kernel(const RowArgs a) {
         if (lane == 0) s_m[warp] = m;
         __syncthreads();
         m = group_max<NW>(s_m[lane & (NW - 1)]);
-        const int64_t ti = tbase >= 0 && m_run == m ? first_index() : kNoIndex;
+        const int64_t ti = holds && m_run == m ? first_index() : kNoIndex;
         const int64_t wi = group_min_i64<32>(ti);
         const float wd = group_sum<32>(dsum * md_factor(m_run, m));
         if (lane == 0) {
@@ -448,11 +496,11 @@ cudaError_t launch_fn(KernelFn k, int64_t grid, int threads, int cs, const RowAr
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-template <Dt DI, int U>
+template <Dt DI, int U, bool PEEL = false>
 cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cudaStream_t st) {
     KernelFn fn = nullptr;
     if (cluster) {
-        if (g == 256) fn = lse_argmax_kernel<DI, 256, U, true>;
+        if (g == 256) fn = lse_argmax_kernel<DI, 256, U, true, PEEL>;
         if (!fn) return cudaErrorInvalidConfiguration;
         if (a.cs > 8) {
             const cudaError_t e =
@@ -462,9 +510,16 @@ cudaError_t launch_lse_u(const RowArgs &a, int g, bool cluster, int64_t grid, cu
         return launch_fn(fn, grid, 256, a.cs, a, st);
     }
 #define OSR_MAKE(G) \
-    if (g == G) fn = lse_argmax_kernel<DI, G, U, false>;
-    OSR_MAKE(1) OSR_MAKE(2) OSR_MAKE(4) OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(64)
-    OSR_MAKE(128) OSR_MAKE(256) OSR_MAKE(512) OSR_MAKE(1024)
+    if (g == G) fn = lse_argmax_kernel<DI, G, U, false, PEEL>;
+    if constexpr (PEEL) {
+        // a lane per edge element: groups of at least U lanes
+        if constexpr (U <= 4) { OSR_MAKE(4) }
+        OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(64) OSR_MAKE(128) OSR_MAKE(256) OSR_MAKE(512)
+        OSR_MAKE(1024)
+    } else {
+        OSR_MAKE(1) OSR_MAKE(2) OSR_MAKE(4) OSR_MAKE(8) OSR_MAKE(16) OSR_MAKE(32) OSR_MAKE(64)
+        OSR_MAKE(128) OSR_MAKE(256) OSR_MAKE(512) OSR_MAKE(1024)
+    }
 #undef OSR_MAKE
     if (!fn) return cudaErrorInvalidConfiguration;
     return launch_fn(fn, grid, g <= 32 ? RowsGeom<1>::kThreads : g, 0, a, st);
@@ -502,7 +557,14 @@ cudaError_t launch_lse(const RowArgs &a, int g, bool cluster, bool vec, int64_t 
     return launch_lse_u<DI, 1>(a, g, cluster, grid, st);
 }
 
+template <Dt DI>
+cudaError_t launch_lse_peel(const RowArgs &a, int g, bool cluster, int64_t grid, cudaStream_t st) {
+    return launch_lse_u<DI, Elem<DI>::kVec, true>(a, g, cluster, grid, st);
+}
+
 template cudaError_t launch_lse<Dt::F32>(const RowArgs &, int, bool, bool, int64_t, cudaStream_t);
+template cudaError_t launch_lse_peel<Dt::F32>(const RowArgs &, int, bool, int64_t, cudaStream_t);
+template cudaError_t launch_lse_peel<Dt::BF16>(const RowArgs &, int, bool, int64_t, cudaStream_t);
 template cudaError_t launch_lse<Dt::BF16>(const RowArgs &, int, bool, bool, int64_t, cudaStream_t);
 template cudaError_t launch_lse_staged<Dt::F32>(const RowArgs &, int64_t, size_t, cudaStream_t);
 template cudaError_t launch_lse_staged<Dt::BF16>(const RowArgs &, int64_t, size_t, cudaStream_t);

@@ -275,7 +275,9 @@ def test_logsumexp_plans_and_validation(lib):
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 55, 152064, "f32") == "lse-cluster g=256 cs=8 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 1, 152064, "bf16") == "lse-staged g=256 cs=16 piece=19008B vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32") == "lse-staged g=256 cs=12 piece=50688B vec"
-    assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32", vec_ok=False) == "lse-cluster g=256 cs=10 scalar"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 152064, "f32", vec_ok=False) == "lse-cluster g=256 cs=10 peel"
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 1024, 50257, "bf16") == "lse-rows g=256 cs=1 peel"  # ragged rows
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, 8, 63, "bf16", vec_ok=False) == "lse-rows g=2 cs=1 scalar"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 2, 3000000, "f32") == "lse-cluster g=256 cs=10 vec"  # pieces too big
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 8192, 32000, "bf16") == "lse-rows g=256 cs=1 vec"
     assert osr.plan_describe(osr.OP_LOGSUMEXP, 100000, 32, "f32") == "lse-rows g=1 cs=1 vec"

@@ -154,6 +154,32 @@ def test_logsumexp_workloads_full_size(name):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("off", [0, 1, 3, 5])
+@pytest.mark.parametrize("M,N", [(3, 50257), (40, 4097), (2000, 1001), (9, 152065), (70, 8200)])
+def test_logsumexp_peeled_rows(M, N, off, dt):
+    # rows that do not start on a 16-byte boundary (a base offset of `off`
+    # elements, or a ragged length): each row's aligned body in vectors, its
+    # head and tail one element a lane -- the cluster, CTA and group forms.
+    # Maxima planted in the head, the tail, and tied across head and tail.
+    x = case(M, N, dt, seed_of("lse-peel", M, N, off, dt)).float()
+    top = 4000.0
+    x[0, 0] = top
+    x[1, N - 1] = top
+    x[2, 1] = top
+    x[2, N - 2] = top
+    x = x.to(DT[dt])
+    buf = torch.empty(M * N + off, dtype=x.dtype, device="cuda")
+    xd = buf[off:].view(M, N)
+    xd.copy_(x.cuda())
+    ragged = off * x.element_size() % 16 != 0 or N % (16 // x.element_size()) != 0
+    assert osr.plan_describe(osr.OP_LOGSUMEXP, M, N, dt, vec_ok=off == 0).endswith("peel" if ragged else "vec")
+    lse, am = osr.row_logsumexp(xd)
+    torch.cuda.synchronize()
+    assert am.cpu().tolist()[:3] == [0, N - 1, 1]
+    check_lse(x, lse, am)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("M", [8, 9, 54, 55, 68, 69, 127, 128, 512])
 def test_logsumexp_plan_boundaries(M, dt):
     # the row counts where the planner changes tier on vocabulary rows:

@@ -20,10 +20,6 @@ def kv(plan, key):
     return int(m.group(1)) if m else None
 
 
-def units(N, dt, vec):
-    return N // (16 // EB[dt]) if vec else N
-
-
 @pytest.fixture(scope="module", autouse=True)
 def lib():
     osr.library()
@@ -32,19 +28,23 @@ def lib():
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("vec", [True, False])
 def test_logsumexp_plans_are_runnable(dt, vec):
-    u = 16 // EB[dt] if vec else 1
     for M in ROWS:
         for N in LENGTHS:
-            if vec and N % u:
-                continue
             plan = osr.plan_describe(osr.OP_LOGSUMEXP, M, N, dt, vec_ok=vec)
+            ragged = not vec or N % (16 // EB[dt])
+            # rows not 16-byte aligned (or ragged) stream peeled bodies from 64 elements on
+            assert plan.endswith("peel" if ragged and N >= 64 else "scalar" if ragged else "vec"), (M, N, plan)
+            body = plan.endswith(("vec", "peel"))
+            u = 16 // EB[dt] if body else 1
             g, cs = kv(plan, "g"), kv(plan, "cs")
             assert g and g & (g - 1) == 0 and 1 <= g <= 1024, plan
             assert cs and 1 <= cs <= 16, plan
-            nunits = units(N, dt, vec)
+            if plan.endswith("peel"):
+                assert g >= u, (M, N, plan)  # a lane per edge element
+            nunits = N // u
             if plan.startswith("lse-staged"):
                 piece = kv(plan, "piece")
-                assert vec and M <= 8 and cs > 1 and 128 + piece <= 200 << 10, (M, N, plan)
+                assert plan.endswith("vec") and M <= 8 and cs > 1 and 128 + piece <= 200 << 10, (M, N, plan)
                 assert cs * piece // 16 >= nunits, (M, N, plan)
             elif plan.startswith("lse-cluster"):
                 assert g == 256 and cs > 1, plan
