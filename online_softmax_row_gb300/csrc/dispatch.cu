@@ -674,7 +674,8 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
             if (c > cs_min && cdiv(N, c) < (int64_t)kTopkThreads * u) break;  // under a vector a thread
             const int64_t ch = cdiv(cdiv(N, c), u) * u;
             if (ch * eb > kTopkMaxPieceBytes) continue;
-            int64_t r = ch * eb > pow2_at_least(k) * 8 ? ch * eb : pow2_at_least(k) * 8;
+            const int64_t cb = ch * eb + (vec ? 0 : 16);
+            int64_t r = cb > pow2_at_least(k) * 8 ? cb : pow2_at_least(k) * 8;
             if (r < kTopkMinWords * 8) r = kTopkMinWords * 8;
             const int64_t sm = (int64_t)topk_smem_bytes((uint32_t)cdiv(r, 16) * 16, k);
             if (sm > kTopkSmemLimit) continue;
@@ -701,8 +702,11 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
     const int64_t chunk = cdiv(cdiv(N, cs), u) * u;
     if (chunk * eb > kTopkMaxPieceBytes) return OSR_ERR_UNSUPPORTED;
     const int64_t sort_n = pow2_at_least(k);
-    // the region holds the piece, and later the gathered lists or the sort
-    int64_t r0 = chunk * eb > sort_n * 8 ? chunk * eb : sort_n * 8;
+    // the region holds the piece (element path: shifted by up to 15 bytes,
+    // as it lies off the 16-byte grid), and later the gathered lists or the
+    // sort
+    const int64_t pb = chunk * eb + (vec ? 0 : 16);
+    int64_t r0 = pb > sort_n * 8 ? pb : sort_n * 8;
     if (r0 < kTopkMinWords * 8) r0 = kTopkMinWords * 8;
     r0 = cdiv(r0, 16) * 16;
     const size_t smem = topk_smem_bytes((uint32_t)r0, k);

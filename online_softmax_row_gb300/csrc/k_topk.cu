@@ -321,11 +321,25 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
             }
         }
     } else {
-        for (int i = tid; i < n; i += kTopkThreads) {
-            const Raw b = xrow[e0 + i];
-            piece[i] = b;
-            tmax = fmaxf(tmax, raw_to_f32(b, DI));
-        }
+        // a piece off the 16-byte grid: placed in shared memory as many bytes
+        // past a boundary as it lies in global memory, so its whole 16-byte
+        // chunks go by cp.async as on the vector path and only the few
+        // elements before the first boundary and after the last are loaded
+        // one by one (the region has 16 bytes to spare for the shift)
+        const char *src = reinterpret_cast<const char *>(xrow + e0);
+        const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(src) & 15u);
+        piece = reinterpret_cast<Raw *>(smem + mis);
+        const int head = (int)(mis ? (16u - mis) / sizeof(Raw) : 0u) < n ? (int)(mis ? (16u - mis) / sizeof(Raw) : 0u) : n;
+        const int nch = (int)((int64_t)(n - head) * (int64_t)sizeof(Raw) / 16);
+        const int t0 = head + nch * (int)(16 / sizeof(Raw));
+        const char *body = src + head * sizeof(Raw);
+        unsigned char *dst = smem + mis + head * sizeof(Raw);  // 16-byte aligned
+        for (int i = tid; i < nch; i += kTopkThreads) cp_async16(smem_u32(dst + i * 16), body + (int64_t)i * 16);
+        for (int i = tid; i < head; i += kTopkThreads) piece[i] = xrow[e0 + i];
+        for (int i = t0 + tid; i < n; i += kTopkThreads) piece[i] = xrow[e0 + i];
+        cp_async_wait_all();
+        __syncthreads();  // every thread's copies have landed
+        for (int i = tid; i < n; i += kTopkThreads) tmax = fmaxf(tmax, raw_to_f32(piece[i], DI));
     }
 
     // ---- a lower bound g of the row's k-th largest element.  With
