@@ -32,7 +32,8 @@
 //              above the k-th largest), finds the k-th largest key T by
 //              8-bit radix passes over it, takes the words above T and the
 //              largest of those equal to T, and writes them in order (values
-//              re-read from the row, columns, the softmax of the k values).
+//              rebuilt from their keys, zeros and NaNs re-read from the row;
+//              columns; the softmax of the k values).
 // When a list overflows (k > 256 gives no bound; heavy ties at the bound) or
 // the union does not fit, the cluster selects together instead: radix passes
 // over the lists or the whole pieces with the histograms summed through
@@ -115,7 +116,9 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Inclusive sum over the CTA's threads in thread order; `scratch` holds
-// kWarps values.  Ends with the CTA synchronised.
+// kWarps values.  With END_SYNC it ends with the CTA synchronised (scratch
+// free again); without, the caller synchronises before reusing scratch.
+template <bool END_SYNC = true>
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t *scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -128,7 +131,7 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t *s
     uint32_t before = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) before += w < warp ? scratch[w] : 0u;
-    __syncthreads();
+    if (END_SYNC) __syncthreads();
     return v + before;
 }
 
@@ -142,13 +145,15 @@ __device__ __forceinline__ float block_max_f(float v, float *scratch) {
     return v;
 }
 
+// The CTA's sum (a fixed tree); END_SYNC as in block_inclusive_scan.
+template <bool END_SYNC = true>
 __device__ __forceinline__ float block_sum_f(float v, float *scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v = group_sum<32>(v);
     if (lane == 0) scratch[warp] = v;
     __syncthreads();
     v = group_sum<kWarps>(scratch[lane & (kWarps - 1)]);
-    __syncthreads();
+    if (END_SYNC) __syncthreads();
     return v;
 }
 
@@ -461,21 +466,26 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         d += __uint_as_float(xstate[r].y) * expf(__uint_as_float(xstate[r].x) - m);
     if (rank == 0 && a.lse != nullptr && tid == 0) a.lse[row] = m + logf(d);
 
-    auto value_at = [&](uint32_t j) {  // the row's own value (an index outside
-        // the row could only come from a selection that found fewer than k
-        // candidates: reported as NaN, never read)
-        return j < (uint32_t)a.N ? raw_to_f32(xrow[j], DI) : __uint_as_float(0x7fc00000u);
-    };
-    auto store = [&](int64_t t, uint32_t j, float p) {
-        a.values[row * k + t] = value_at(j);
-        a.indices[row * k + t] = j < (uint32_t)a.N ? (int64_t)j : -1;
+    // The row's own value of a word.  A key stands for one bit pattern except
+    // the keys of zero (+0 and -0) and of NaN (every NaN): those two are
+    // re-read from the row (in L2), the rest rebuilt from the key.  An index
+    // outside the row could only come from a selection that found fewer than
+    // k candidates: reported as NaN, never read.
+    const uint32_t zero_key = topk_key(0u, DI), nan_key = topk_key(DI == Dt::BF16 ? 0x7fc0u : 0x7fc00000u, DI);
+    auto store = [&](int64_t t, uint64_t w, float p) {
+        const uint32_t key = (uint32_t)(w >> 32), j = inv - (uint32_t)w;
+        const bool in_row = j < (uint32_t)a.N;
+        a.values[row * k + t] = !in_row ? __uint_as_float(0x7fc00000u)
+                                : key == zero_key || key == nan_key ? raw_to_f32(xrow[j], DI)
+                                                                    : key_value<DI>(key);
+        a.indices[row * k + t] = in_row ? (int64_t)j : -1;
         if (a.probs != nullptr) a.probs[row * k + t] = p;
     };
     // Radix selection of the k-th largest key T among keys delivered by
-    // `each` (8 bits per pass from the top).  `merge` turns this CTA's
-    // histogram into the one the choice is made from (the cluster's sum, or
-    // the CTA's own); returns T and leaves in krem how many keys equal to T
-    // belong to the k largest.
+    // `each` (8 bits per pass from the top).  `merge(b)` gives the count of
+    // digit b in the histogram the choice is made from (the cluster's sum,
+    // or the CTA's own); returns T and leaves in krem how many keys equal to
+    // T belong to the k largest.
     uint32_t krem = (uint32_t)k;
     auto radix_select = [&](auto &&each, auto &&merge) {
         uint32_t prefix = 0;
@@ -489,14 +499,13 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
                 if (p == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
             });
             __syncthreads();
-            const uint32_t H = merge(hist[tid]);
-            __syncthreads();
             // S_b = keys in play with digit >= b, an inclusive scan in
             // descending digit order: thread t takes digit 255 - t
-            hist[255 - tid] = H;
-            __syncthreads();
-            const uint32_t Hr = hist[tid];
-            const uint32_t S = block_inclusive_scan(Hr, s_scan);
+            const uint32_t Hr = merge(255 - tid);
+            // s_scan, s_bin and s_krem are next written after at least two
+            // more barriers, which every reader passes first: no barrier
+            // closes the scan or the pass
+            const uint32_t S = block_inclusive_scan<false>(Hr, s_scan);
             if (S >= krem && S - Hr < krem) {
                 s_bin = 255u - (uint32_t)tid;
                 s_krem = krem - (S - Hr);
@@ -504,7 +513,6 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
             __syncthreads();
             prefix = (prefix << 8) | s_bin;
             krem = s_krem;
-            __syncthreads();
         }
         return prefix;
     };
@@ -529,17 +537,17 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
             fail();
             return;
         }
-        __syncthreads();
+        // every thread has read the list length; the radix passes' barriers
+        // order this reset before the gathering below
+        if (tid == 0) list_n = 0;
         auto each_u = [&](auto &&f) {
             for (uint32_t i = tid; i < total; i += kTopkThreads) f((uint32_t)(words[i] >> 32), (int64_t)i);
         };
-        const uint32_t T = radix_select(each_u, [](uint32_t h) { return h; });
+        const uint32_t T = radix_select(each_u, [&](int b) { return hist[b]; });
         // keys above T, and the krem largest words among those equal to T
         // (equal keys: the smaller columns; every word differs).  The equal
         // words are gathered into `list` (free now) and ranked among
         // themselves.
-        if (tid == 0) list_n = 0;
-        __syncthreads();
         for (uint32_t i = tid; i < total; i += kTopkThreads) {
             const uint64_t w = words[i];
             const uint32_t key = (uint32_t)(w >> 32);
@@ -586,13 +594,13 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         };
         int xb = 0;
         uint32_t *pub = nullptr;
-        auto cluster_merge = [&](uint32_t h) {
+        auto cluster_merge = [&](int b) {
             pub = hist_pub + xb * 256;
-            pub[tid] = h;
+            pub[tid] = hist[tid];
             xb ^= 1;
             cluster_sync_all();
             uint32_t H = 0;
-            for (int r = 0; r < cs; ++r) H += ld_dsmem_u32(mapa_shared(smem_u32(pub + tid), r));
+            for (int r = 0; r < cs; ++r) H += ld_dsmem_u32(mapa_shared(smem_u32(pub + b), r));
             return H;
         };
         const uint32_t T = radix_select(each, cluster_merge);
@@ -639,30 +647,31 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         }
     }
     __syncthreads();
-    if (in_cand) {
-        for (int i = tid; i < k; i += kTopkThreads) words[i] = cand[i];
-        __syncthreads();
-    }
 
-    // ---- CTA 0 writes the k words in order: values re-read from the row,
-    //      columns, the softmax of the k values (largest first, so v0 is their
-    //      maximum), summed in output order
+    // ---- CTA 0 writes the k words in order: values, columns, the softmax of
+    //      the k values (largest first, so v0 is their maximum), summed in
+    //      output order
     if (k <= kTopkRankMaxK) {
         // output position = the number of larger words (all words differ)
+        const uint64_t *kw = in_cand ? cand : words;
         int64_t t = 0;
         uint64_t w = 0;
         if (tid < k) {
-            w = words[tid];
-            for (int j = 0; j < k; ++j) t += words[j] > w;
+            w = kw[tid];
+            for (int j = 0; j < k; ++j) t += kw[j] > w;
             if (t == 0) s_top = w;
         }
         __syncthreads();
         const float v0 = key_value<DI>((uint32_t)(s_top >> 32));  // the largest value
         if (tid < k) s_ez[t] = expf(key_value<DI>((uint32_t)(w >> 32)) - v0);
         __syncthreads();
-        const float rz = __frcp_rn(block_sum_f(tid < k ? s_ez[tid] : 0.f, s_red));
-        if (tid < k) store(t, inv - (uint32_t)w, s_ez[t] * rz);
+        const float rz = __frcp_rn(block_sum_f<false>(tid < k ? s_ez[tid] : 0.f, s_red));
+        if (tid < k) store(t, w, s_ez[t] * rz);
     } else {
+        if (in_cand) {
+            for (int i = tid; i < k; i += kTopkThreads) words[i] = cand[i];
+            __syncthreads();
+        }
         // a bitonic network on a.sort_n >= k words (zero words sort last)
         for (int i = (int)k + tid; i < a.sort_n; i += kTopkThreads) words[i] = 0ull;
         __syncthreads();
@@ -685,7 +694,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const TopkArgs a)
         for (int t = tid; t < k; t += kTopkThreads) z += expf(key_value<DI>((uint32_t)(words[t] >> 32)) - v0);
         const float rz = __frcp_rn(block_sum_f(z, s_red));
         for (int t = tid; t < k; t += kTopkThreads)
-            store(t, inv - (uint32_t)words[t], expf(key_value<DI>((uint32_t)(words[t] >> 32)) - v0) * rz);
+            store(t, words[t], expf(key_value<DI>((uint32_t)(words[t] >> 32)) - v0) * rz);
     }
     pdl_trigger();
 }

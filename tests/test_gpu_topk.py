@@ -48,6 +48,9 @@ def check(x_cpu, k, values, indices, probs, lse, what=""):
     gv = values.cpu().numpy().astype(np.float64).reshape(r_v.shape)
     same = (gv == r_v) | (np.isnan(gv) & np.isnan(r_v))
     assert same.all(), f"{what}: values differ"
+    # the row's own numbers: -0 stays -0 (== does not tell it from +0)
+    num = ~np.isnan(r_v)
+    assert np.array_equal(np.signbit(gv[num]), np.signbit(r_v[num])), f"{what}: signs of zero differ"
     if probs is not None:
         check_f32_abs(probs.reshape(r_p.shape), r_p, 1e-6, 1e-5, f"{what} probs")
     if lse is not None:
@@ -168,14 +171,17 @@ def test_topk_workload_full_size():
 def test_topk_constant_rows(spec):
     # every element equal: the k smallest columns.  With two CTAs of 1000
     # elements each the lists fit but all 2000 words tie (more than a
-    # gathered list holds); with one CTA the list itself overflows.
-    x = torch.full((3, 2000), 1.5, dtype=torch.bfloat16)
+    # gathered list holds); with one CTA the list itself overflows.  Row 3
+    # alternates -0 and +0 (equal numbers, each returned with its own sign).
+    x = torch.full((4, 2000), 1.5, dtype=torch.bfloat16)
     x[1] = -2.0
+    x[3] = torch.tensor([-0.0, 0.0] * 1000)
     fn = lambda: osr.row_topk(x.cuda(), 50)
     out = run_forced(spec, fn) if spec else fn()
     torch.cuda.synchronize()
     check(x, 50, *out, what=f"constant {spec or 'default'}")
-    assert out[1].cpu().tolist() == [list(range(50))] * 3
+    assert out[1].cpu().tolist() == [list(range(50))] * 4
+    assert torch.signbit(out[0][3]).cpu().tolist() == [True, False] * 25
 
 
 def test_topk_on_pinned_host_rows():
