@@ -652,6 +652,22 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
     int64_t cs = cs_min;
     const ForceSpec force_spec = forced_spec();
     const char *force = force_spec.get();
+    // CTAs of c a row that an SM holds by shared memory (at most 4, the
+    // register bound); 0 if a piece of that size does not fit
+    auto per_sm = [&](int64_t c) -> int64_t {
+        const int64_t ch = cdiv(cdiv(N, c), u) * u;
+        if (ch * eb > kTopkMaxPieceBytes) return 0;
+        const int64_t cb = ch * eb + (vec ? 0 : 16);
+        int64_t r = cb > pow2_at_least(k) * 8 ? cb : pow2_at_least(k) * 8;
+        if (r < kTopkMinWords * 8) r = kTopkMinWords * 8;
+        const int64_t sm = (int64_t)topk_smem_bytes((uint32_t)cdiv(r, 16) * 16, k);
+        if (sm > kTopkSmemLimit) return 0;
+        const int64_t per = smem_per_sm / (sm + kTopkStaticSmem + 1024);  // 1 KiB reserved a CTA
+        return per > 4 ? 4 : per;
+    };
+    // c CTAs a row leave at least a vector a thread (or c is the fewest the row needs)
+    auto enough_work = [&](int64_t c) { return c == cs_min || cdiv(N, c) >= (int64_t)kTopkThreads * u; };
+    const int64_t c_max = kTopkMaxCluster < max_cluster ? kTopkMaxCluster : max_cluster;
     int64_t fcs = 0;
     if (force && strncmp(force, "topk", 4) == 0) {
         if (!parse_kv(force, "cs", &fcs) || fcs < 1) return OSR_ERR_UNSUPPORTED;
@@ -660,27 +676,18 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
     } else if (M > 96) {
         // many rows: each CTA's time is mostly a chain of short phases, so
         // what counts is how many rows an SM works on at once -- the CTAs an
-        // SM holds by shared memory (at most 4, the register bound) over the
-        // CTAs a row needs; on a tie, the fewest CTAs a row that still puts
-        // two on an SM (a lone CTA an SM leaves its copy and phases
-        // unoverlapped: 262144 bf16 elements at 3 CTAs a row, one an SM,
-        // 0.28 against 0.33 at 6, two an SM).  Measured at 512-2048
+        // SM holds over the CTAs a row needs; on a tie, the fewest CTAs a row
+        // that still puts two on an SM (a lone CTA an SM leaves its copy and
+        // phases unoverlapped: 262144 bf16 elements at 3 CTAs a row, one an
+        // SM, 0.28 against 0.33 at 6, two an SM).  Measured at 512-2048
         // rows (fraction of the copy peak, against the 6 CTAs a row before):
         // bf16 152064 elements 3 CTAs 0.34 against 0.31, 65536 elements 3
         // 0.33 against 0.20, 32768 elements 2 0.24 against 0.11; fp32 32768
         // elements 3 0.35 against 0.21; fp32 152064 and bf16 262144 stay at 6.
         int64_t best = 0, best_per = 0;
-        for (int64_t c = cs_min; c <= kTopkMaxCluster && c <= max_cluster; ++c) {
-            if (c > cs_min && cdiv(N, c) < (int64_t)kTopkThreads * u) break;  // under a vector a thread
-            const int64_t ch = cdiv(cdiv(N, c), u) * u;
-            if (ch * eb > kTopkMaxPieceBytes) continue;
-            const int64_t cb = ch * eb + (vec ? 0 : 16);
-            int64_t r = cb > pow2_at_least(k) * 8 ? cb : pow2_at_least(k) * 8;
-            if (r < kTopkMinWords * 8) r = kTopkMinWords * 8;
-            const int64_t sm = (int64_t)topk_smem_bytes((uint32_t)cdiv(r, 16) * 16, k);
-            if (sm > kTopkSmemLimit) continue;
-            int64_t per = smem_per_sm / (sm + kTopkStaticSmem + 1024);  // 1 KiB reserved a CTA
-            if (per > 4) per = 4;
+        for (int64_t c = cs_min; c <= c_max; ++c) {
+            if (!enough_work(c)) break;
+            const int64_t per = per_sm(c);
             if (per == 0) continue;
             if (best == 0 || per * best > best_per * c || (per * best == best_per * c && best_per < 2 && per > best_per)) {
                 best = c;
@@ -691,12 +698,42 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
     } else {
         // measured on 1-96 rows of 152064 elements: 8 CTAs per row for up to
         // 16 rows (3-5 % faster than 12 with the row-wide bound, 7-11 %
-        // faster than 16), 4 up to 96 rows (10 % faster than 8 at 64); never
+        // faster than 16), 4 up to 96 rows (64 bf16 rows: 14.2 us against
+        // 14.4 at 2, 15.3 at 3, 15.8 at 5, 15.0 at 6, 16.2 at 8); never
         // fewer than the row needs, and never so many that a CTA gets less
         // than one vector per thread
         const int64_t fill = M <= 16 ? 8 : 4;
         if (fill > cs) cs = fill;
         while (cs > cs_min && cdiv(N, cs) < (int64_t)kTopkThreads * u) cs = cs / 2 > cs_min ? cs / 2 : cs_min;
+        // ... as long as the grid stays one wave: past it, the most CTAs a
+        // row below that still fit (96 bf16 rows: 4 CTAs a row, 384 CTAs at
+        // two an SM, 23.1 us; 3 a row 16.6 us).  Where no size fits (64 fp32
+        // rows of 152064 elements), the size with the fewest CTAs per
+        // resident slot, the larger on a tie (4 a row, one an SM: 25.9 us;
+        // 5, one an SM: 28.7; 6, two an SM: 23.6; 8, two an SM: 24.9).
+        auto fits = [&](int64_t c) {
+            const int64_t per = per_sm(c);
+            return per > 0 && M * c <= per * (int64_t)sms;
+        };
+        if (!fits(cs)) {
+            int64_t c = cs - 1;
+            while (c >= cs_min && !fits(c)) --c;
+            if (c >= cs_min) {
+                cs = c;
+            } else {
+                int64_t best = 0, best_per = 0;
+                for (int64_t c2 = cs_min; c2 <= c_max; ++c2) {
+                    if (!enough_work(c2)) break;
+                    const int64_t per = per_sm(c2);
+                    if (per == 0) continue;
+                    if (best == 0 || c2 * best_per <= best * per) {  // c2 / per <= best / best_per
+                        best = c2;
+                        best_per = per;
+                    }
+                }
+                if (best > 0) cs = best;
+            }
+        }
     }
     if (cs > max_cluster || cs > kTopkMaxCluster) return OSR_ERR_UNSUPPORTED;
     const int64_t chunk = cdiv(cdiv(N, cs), u) * u;

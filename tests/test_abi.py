@@ -312,7 +312,14 @@ def test_topk_plans_and_validation(lib, force):
     assert D(osr.OP_TOPK, 2048, 32768, "bf16") == "topk cs=1 piece=65536B vec"
     assert D(osr.OP_TOPK, 2048, 65536, "bf16") == "topk cs=3 piece=43696B vec"
     assert D(osr.OP_TOPK, 2048, 262144, "bf16") == "topk cs=6 piece=87392B vec"
-    assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=4 piece=152064B vec"
+    # few rows: 4 CTAs a row while the grid stays one wave (two CTAs an SM
+    # at 76 KiB pieces: 76 rows), then fewer; with no size fitting one wave,
+    # the fewest CTAs per resident slot
+    assert D(osr.OP_TOPK, 76, 152064, "bf16") == "topk cs=4 piece=76032B vec"
+    assert D(osr.OP_TOPK, 77, 152064, "bf16") == "topk cs=3 piece=101376B vec"
+    assert D(osr.OP_TOPK, 96, 152064, "bf16") == "topk cs=3 piece=101376B vec"
+    assert D(osr.OP_TOPK, 32, 152064, "f32") == "topk cs=4 piece=152064B vec"
+    assert D(osr.OP_TOPK, 64, 152064, "f32") == "topk cs=6 piece=101376B vec"
     assert D(osr.OP_TOPK, 8, 1000, "bf16") == "topk cs=1 piece=2000B vec"       # short rows: one CTA
     assert D(osr.OP_TOPK, 3, 33, "bf16", vec_ok=False) == "topk cs=1 piece=66B scalar"
     assert D(osr.OP_TOPK, 1, 786432, "f32") == "topk cs=16 piece=196608B vec"   # largest row
