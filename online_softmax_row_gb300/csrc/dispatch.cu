@@ -696,13 +696,15 @@ osr_status topk_plan(int64_t M, int64_t N, int64_t k, osr_dtype dt, bool vec, in
         }
         if (best > 0) cs = best;
     } else {
-        // measured on 1-96 rows of 152064 elements: 8 CTAs per row for up to
-        // 16 rows (3-5 % faster than 12 with the row-wide bound, 7-11 %
-        // faster than 16), 4 up to 96 rows (64 bf16 rows: 14.2 us against
-        // 14.4 at 2, 15.3 at 3, 15.8 at 5, 15.0 at 6, 16.2 at 8); never
-        // fewer than the row needs, and never so many that a CTA gets less
-        // than one vector per thread
-        const int64_t fill = M <= 16 ? 8 : 4;
+        // measured on 1-96 rows of 152064 elements: 8 CTAs per row while the
+        // clusters still spread one CTA an SM (up to 15 rows on 152 SMs;
+        // 3-5 % faster than 12, 7-11 % faster than 16, 2-8 % faster than
+        // 6), then 6 (16-22 rows: 2-5 % faster than 8 or 4; at 24 rows 4 %
+        // slower than 4), then 4 up to 96 rows (64 bf16 rows: 14.2 us
+        // against 14.4 at 2, 15.3 at 3, 15.8 at 5, 15.0 at 6, 16.2 at 8);
+        // never fewer than the row needs, and never so many that a CTA gets
+        // less than one vector per thread
+        const int64_t fill = M * 8 <= (int64_t)sms * 4 / 5 ? 8 : M * 6 <= (int64_t)sms * 7 / 8 ? 6 : 4;
         if (fill > cs) cs = fill;
         while (cs > cs_min && cdiv(N, cs) < (int64_t)kTopkThreads * u) cs = cs / 2 > cs_min ? cs / 2 : cs_min;
         // ... as long as the grid stays one wave: past it, the most CTAs a

@@ -306,6 +306,10 @@ def test_topk_plans_and_validation(lib, force):
     D = osr.plan_describe
     assert D(osr.OP_TOPK, 64, 152064, "bf16") == "topk cs=4 piece=76032B vec"
     assert D(osr.OP_TOPK, 1, 152064, "bf16") == "topk cs=8 piece=38016B vec"    # few rows: 8 CTAs
+    assert D(osr.OP_TOPK, 15, 152064, "bf16") == "topk cs=8 piece=38016B vec"   # one CTA an SM
+    assert D(osr.OP_TOPK, 16, 152064, "f32") == "topk cs=6 piece=101376B vec"   # then 6 a row
+    assert D(osr.OP_TOPK, 22, 152064, "bf16") == "topk cs=6 piece=50688B vec"
+    assert D(osr.OP_TOPK, 23, 152064, "bf16") == "topk cs=4 piece=76032B vec"
     # many rows: the cluster size that keeps the most rows in flight per SM
     assert D(osr.OP_TOPK, 256, 152064, "bf16") == "topk cs=3 piece=101376B vec"
     assert D(osr.OP_TOPK, 256, 152064, "f32") == "topk cs=6 piece=101376B vec"

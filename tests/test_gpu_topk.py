@@ -76,12 +76,14 @@ def test_topk(M, N, k, dt):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("M,N,k", [(64, 152064, 50), (80, 152064, 50), (96, 152064, 50), (97, 152064, 50),
-                                   (130, 152064, 50), (200, 32768, 50), (120, 65536, 64), (98, 5000, 8)])
+@pytest.mark.parametrize("M,N,k", [(15, 152064, 50), (20, 152064, 50), (64, 152064, 50), (80, 152064, 50),
+                                   (96, 152064, 50), (97, 152064, 50), (130, 152064, 50), (200, 32768, 50),
+                                   (120, 65536, 64), (98, 5000, 8)])
 def test_topk_many_rows(M, N, k, dt):
-    # up to 96 rows, the one-wave cluster sizes (64 rows: 4 CTAs a row in
-    # bf16, 6 in fp32; 80 and 96 rows: 3 in bf16); beyond, the planner's
-    # rows-in-flight sizes (1, 3 or 6 CTAs a row here); every row checked
+    # up to 96 rows, the planner's few-row sizes (15 rows: 8 CTAs a row; 20
+    # rows: 6; 64 rows: 4 in bf16, 6 in fp32; 80 and 96 rows: 3 in bf16);
+    # beyond, its rows-in-flight sizes (1, 3 or 6 CTAs a row here); every
+    # row checked
     x = rows(M, N, dt, seed=M * 7 + N + k)
     out = osr.row_topk(x.cuda(), k)
     torch.cuda.synchronize()
