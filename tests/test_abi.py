@@ -310,6 +310,9 @@ def test_topk_plans_and_validation(lib, force):
     assert D(osr.OP_TOPK, 16, 152064, "f32") == "topk cs=6 piece=101376B vec"   # then 6 a row
     assert D(osr.OP_TOPK, 22, 152064, "bf16") == "topk cs=6 piece=50688B vec"
     assert D(osr.OP_TOPK, 23, 152064, "bf16") == "topk cs=4 piece=76032B vec"
+    # the thresholds follow the SM count: half the SMs, half the rows
+    assert [D(osr.OP_TOPK, m, 152064, "bf16", sm_count=76).split()[1] for m in (7, 8, 11, 12, 38, 39)] == \
+        ["cs=8", "cs=6", "cs=6", "cs=4", "cs=4", "cs=3"]
     # many rows: the cluster size that keeps the most rows in flight per SM
     assert D(osr.OP_TOPK, 256, 152064, "bf16") == "topk cs=3 piece=101376B vec"
     assert D(osr.OP_TOPK, 256, 152064, "f32") == "topk cs=6 piece=101376B vec"
